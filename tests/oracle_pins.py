@@ -1,0 +1,260 @@
+"""Pin checks for the GEMM oracle, written as plain functions so that the tests can
+run them on the oracle as it is and on deliberately broken copies of it (a pin that
+cannot tell a broken oracle from the real one pins nothing).
+
+The independent evaluator here works element by element with exact rationals
+(``fractions.Fraction``), decodes E4M3 and UE8M0 from their bit fields and reads the
+packed scale words with integer shifts.  It shares no code with ``oracle/``."""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+# ------------------------------------------------------------- exact decode
+def fr_e4m3(code: int) -> Fraction:
+    code = int(code)
+    s, e, m = code >> 7, (code >> 3) & 15, code & 7
+    assert not (e == 15 and m == 7), "NaN code in brute-force input"
+    mag = Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return -mag if s else mag
+
+
+def fr_ue8(byte: int) -> Fraction:
+    assert byte != 255
+    return Fraction(2) ** (int(byte) - 127)
+
+
+def word_byte(words: np.ndarray, group: int, index: int) -> int:
+    w = int(np.asarray(words).view(np.uint32)[group // 4, index])
+    return (w >> (8 * (group % 4))) & 0xFF
+
+
+def fr_to_bf16_bits(x: Fraction) -> int:
+    """Exact round-to-nearest-even of a rational to BF16 bits (finite range only)."""
+    if x == 0:
+        return 0
+    sign = 0x8000 if x < 0 else 0
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)
+    q = a / Fraction(2) ** (e - 7)
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    val = fl * Fraction(2) ** (e - 7)
+    f32 = np.float32(float(val))          # exactly representable
+    return sign | int(np.array([f32]).view(np.uint32)[0] >> 16)
+
+
+# -------------------------------------------------------- exact references
+def exact_dense(a, sfa, b, sfb, c, m, n) -> Fraction:
+    k = a.shape[1]
+    tot = Fraction(0) if c is None else Fraction(float(c[m, n]))
+    for kk in range(k):
+        g = kk // 128
+        tot += (fr_e4m3(a[m, kk]) * fr_ue8(word_byte(sfa, g, m)) *
+                fr_e4m3(b[n, kk]) * fr_ue8(word_byte(sfb, g, n // 128)))
+    return tot
+
+
+def exact_k_grouped(a, sfa, b, sfb, ks, c, e, m, n) -> Fraction:
+    off = int(sum(ks[:e]))
+    tot = Fraction(0) if c is None else Fraction(float(c[e, m, n]))
+    for kk in range(off, off + int(ks[e])):
+        g = kk // 128
+        tot += (fr_e4m3(a[kk, m]) * fr_ue8(word_byte(sfa, g, m)) *
+                fr_e4m3(b[kk, n]) * fr_ue8(word_byte(sfb, g, n)))
+    return tot
+
+
+# ------------------------------------------------------------ input makers
+def rand_codes(g, shape):
+    q = g.integers(0, 256, shape, dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x38        # no NaN in valid data
+    return q
+
+
+def rand_words(g, mn, groups, lo=118, hi=137):
+    from oracle.formats import pack_ue8m0   # packing is pinned by its own golden test
+    return pack_ue8m0(g.integers(lo, hi, (mn, groups), dtype=np.uint8))
+
+
+def close_fp64(got: float, exact: Fraction, mag: Fraction, k: int) -> bool:
+    return abs(Fraction(got) - exact) <= mag * k * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 1000)
+
+
+# ------------------------------------------------------------------- checks
+def check_golden_gemm():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    for case in GOLDEN["gemm_nt"]:
+        m, n, k = case["M"], case["N"], case["K"]
+        a = np.full((m, k), int(case["a"], 16), np.uint8)
+        b = np.full((n, k), int(case["b"], 16), np.uint8)
+        sfa = pack_ue8m0(np.tile(np.array(case["sa"], np.uint8), (m, 1)))
+        sfb = pack_ue8m0(np.tile(np.array(case["sb"], np.uint8), ((n + 127) // 128, 1)))
+        c = None if case["c"] is None else np.full((m, n), case["c"], np.float32)
+        d = oracle.fp8_gemm_nt(a, sfa, b, sfb, c)
+        assert np.all(d == case["expect"]), (case["name"], d)
+
+
+def check_dense_brute_force(seed=0):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    for (m, n, k, with_c) in [(3, 5, 128, False), (2, 131, 384, True), (4, 7, 640, False)]:
+        a, b = rand_codes(g, (m, k)), rand_codes(g, (n, k))
+        sfa, sfb = rand_words(g, m, k // 128), rand_words(g, (n + 127) // 128, k // 128)
+        c = g.standard_normal((m, n)).astype(np.float32) if with_c else None
+        d = oracle.fp8_gemm_nt(a, sfa, b, sfb, c)
+        bits = oracle.round_output(d, "bf16")
+        cols = range(n) if n < 16 else [0, 1, 64, 127, 128, 129, 130]
+        for i in range(m):
+            for j in cols:
+                ex = exact_dense(a, sfa, b, sfb, c, i, j)
+                mag = sum(abs(fr_e4m3(a[i, kk]) * fr_e4m3(b[j, kk])) for kk in range(k)) * Fraction(2) ** 40
+                assert close_fp64(d[i, j], ex, mag, k), (m, n, k, i, j)
+                assert bits[i, j] == fr_to_bf16_bits(ex), (i, j)
+
+
+def check_contiguous_brute_force(seed=1):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, n, k = 3, 9, 256
+    m_indices = np.array([0, 0, 0, -1, 2, 2, -1, -1, 1, -1], dtype=np.int32)
+    m_total = len(m_indices)
+    a = rand_codes(g, (m_total, k))
+    b = rand_codes(g, (num_groups, n, k))
+    sfa = rand_words(g, m_total, k // 128)
+    sfb = np.stack([rand_words(g, 1, k // 128) for _ in range(num_groups)])
+    d, written = oracle.m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices)
+    assert list(written) == [e >= 0 for e in m_indices]
+    for i in range(m_total):
+        e = m_indices[i]
+        if e < 0:
+            assert np.all(np.isnan(d[i]))
+            continue
+        for j in range(n):
+            ex = exact_dense(a, sfa, b[e], sfb[e], None, i, j)
+            assert float(ex) == d[i, j] or abs(Fraction(d[i, j]) - ex) <= abs(ex) * Fraction(1, 2 ** 45)
+
+
+def check_masked_brute_force(seed=2):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, m_max, n, k = 3, 6, 5, 256
+    masked_m = np.array([0, 6, 2])
+    a = rand_codes(g, (num_groups, m_max, k))
+    b = rand_codes(g, (num_groups, n, k))
+    sfa = np.stack([rand_words(g, m_max, k // 128) for _ in range(num_groups)])
+    sfb = np.stack([rand_words(g, 1, k // 128) for _ in range(num_groups)])
+    out = oracle.m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, masked_m)
+    for e in range(num_groups):
+        assert out[e].shape == (masked_m[e], n)
+        for i in range(masked_m[e]):
+            for j in range(n):
+                ex = exact_dense(a[e], sfa[e], b[e], sfb[e], None, i, j)
+                assert abs(Fraction(out[e][i, j]) - ex) <= abs(ex) * Fraction(1, 2 ** 45) + Fraction(1, 2 ** 900)
+
+
+def check_k_grouped_brute_force(seed=3):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    m, n = 5, 6
+    ks = [256, 0, 128, 384]
+    k_total = sum(ks)
+    a = rand_codes(g, (k_total, m))
+    b = rand_codes(g, (k_total, n))
+    sfa = rand_words(g, m, k_total // 128)
+    sfb = rand_words(g, n, k_total // 128)
+    c = g.standard_normal((len(ks), m, n)).astype(np.float32)
+    out = oracle.k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, ks, c)
+    assert np.array_equal(out[1], c[1].astype(np.float64))      # empty segment: D = C
+    for e in range(len(ks)):
+        for i in range(m):
+            for j in range(n):
+                ex = exact_k_grouped(a, sfa, b, sfb, ks, c, e, i, j)
+                assert abs(Fraction(out[e][i, j]) - ex) <= (abs(ex) + 1) * Fraction(1, 2 ** 45)
+
+
+def check_identity():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    g = np.random.Generator(np.random.PCG64(4))
+    a = np.zeros((128, 128), np.uint8)
+    np.fill_diagonal(a, 0x38)
+    b = rand_codes(g, (200, 128))
+    sfa = pack_ue8m0(np.full((128, 1), 127, np.uint8))
+    sfb_bytes = np.array([[121], [133]], np.uint8)
+    d = oracle.fp8_gemm_nt(a, sfa, b, pack_ue8m0(sfb_bytes))
+    want = np.array([[float(fr_e4m3(b[j, i]) * fr_ue8(sfb_bytes[j // 128, 0])) for j in range(200)]
+                     for i in range(128)])
+    assert np.array_equal(d, want)
+
+
+def check_one_hot():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    a = np.zeros((4, 256), np.uint8)
+    b = np.zeros((3, 256), np.uint8)
+    a[2, 200] = 0x4D     # 1.625 * 2^2 = 6.5 ... e=9, m=5
+    b[1, 200] = 0xB3     # -(1.375) * 2^-1
+    sa = np.full((4, 2), 127, np.uint8)
+    sa[2, 1] = 131
+    sb = np.full((1, 2), 127, np.uint8)
+    sb[0, 1] = 120
+    d = oracle.fp8_gemm_nt(a, pack_ue8m0(sa), b, pack_ue8m0(sb))
+    want = np.zeros((4, 3))
+    want[2, 1] = float(fr_e4m3(0x4D) * fr_e4m3(0xB3) * Fraction(2) ** 4 * Fraction(2) ** -7)
+    assert np.array_equal(d, want)
+    assert oracle.round_output(d, "bf16")[2, 1] == fr_to_bf16_bits(Fraction(want[2, 1]))
+
+
+def scale_probe_inputs(m, n, groups):
+    """A = B = 1.0 everywhere; scale exponents chosen so that every output is a sum
+    of `groups` powers of two whose exponents identify (row, n-block, group)."""
+    ea = np.array([[(i * 5 + gg * 7) % 13 - 6 for gg in range(groups)] for i in range(m)])
+    eb = np.array([[(j * 3 + gg * 11) % 7 - 3 for gg in range(groups)] for j in range((n + 127) // 128)])
+    return ea, eb
+
+
+def check_scale_probe():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    m, n, groups = 40, 300, 6
+    ea, eb = scale_probe_inputs(m, n, groups)
+    a = np.full((m, groups * 128), 0x38, np.uint8)
+    b = np.full((n, groups * 128), 0x38, np.uint8)
+    d = oracle.fp8_gemm_nt(a, pack_ue8m0((ea + 127).astype(np.uint8)), b,
+                           pack_ue8m0((eb + 127).astype(np.uint8)))
+    for i in range(0, m, 3):
+        for j in range(0, n, 17):
+            want = sum(Fraction(2) ** (7 + ea[i, gg] + eb[j // 128, gg]) for gg in range(groups))
+            assert Fraction(d[i, j]) == want, (i, j)
+
+
+def check_integer_valued():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    g = np.random.Generator(np.random.PCG64(12))
+    vals = {-1: 0xB8, 0: 0x00, 1: 0x38}
+    ai = g.integers(-1, 2, (16, 128))
+    bi = g.integers(-1, 2, (24, 128))
+    a = np.vectorize(vals.get)(ai).astype(np.uint8)
+    b = np.vectorize(vals.get)(bi).astype(np.uint8)
+    one = pack_ue8m0(np.full((16, 1), 127, np.uint8))
+    d = oracle.fp8_gemm_nt(a, one, b, pack_ue8m0(np.full((1, 1), 127, np.uint8)))
+    assert np.array_equal(d, (ai @ bi.T).astype(np.float64))
+
+
+ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_contiguous_brute_force,
+              check_masked_brute_force, check_k_grouped_brute_force, check_identity,
+              check_one_hot, check_scale_probe, check_integer_valued]

@@ -1,0 +1,145 @@
+"""Pins for the GEMM oracle: exact rational brute force on tiny shapes, closed forms
+(identity, one-hot, integer-valued, scale identification), the hand-derived fixtures
+of tests/golden/closed_forms.json, and segment logic.  The mutation test plants
+plausible mistakes in a copy of the oracle (on the CPU) and checks that the pins
+catch every one of them."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import formats as F
+from oracle import gemm as G
+import oracle_pins as P
+
+
+@pytest.mark.parametrize("check", P.ALL_CHECKS, ids=lambda f: f.__name__)
+def test_pin(check):
+    check()
+
+
+def test_contiguous_rows_left_untouched_and_expert_routing():
+    g = np.random.Generator(np.random.PCG64(21))
+    m_indices = np.array([1] * 3 + [-1] * 125 + [0] * 128, dtype=np.int32)
+    a = P.rand_codes(g, (256, 128))
+    b = P.rand_codes(g, (2, 16, 128))
+    sfa = P.rand_words(g, 256, 1)
+    sfb = np.stack([P.rand_words(g, 1, 1) for _ in range(2)])
+    d, written = oracle.m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices)
+    assert written.sum() == 131
+    dense1 = oracle.fp8_gemm_nt(a[:3], F.pack_ue8m0(F.unpack_ue8m0(sfa, 256, 1)[:3]), b[1], sfb[1])
+    assert np.array_equal(d[:3], dense1)
+
+
+def test_masked_zero_and_full_masks():
+    g = np.random.Generator(np.random.PCG64(22))
+    a = P.rand_codes(g, (2, 130, 128))
+    b = P.rand_codes(g, (2, 8, 128))
+    sfa = np.stack([P.rand_words(g, 130, 1) for _ in range(2)])
+    sfb = np.stack([P.rand_words(g, 1, 1) for _ in range(2)])
+    out = oracle.m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, [0, 130])
+    assert out[0].shape == (0, 8) and out[1].shape == (130, 8)
+    assert np.array_equal(out[1], oracle.fp8_gemm_nt(a[1], sfa[1], b[1], sfb[1]))
+
+
+def test_k_grouped_equals_dense_on_one_segment():
+    # one expert over the whole K: the TN GEMM equals the NT GEMM of the transposes
+    g = np.random.Generator(np.random.PCG64(23))
+    k, m, n = 256, 7, 9
+    a = P.rand_codes(g, (k, m))
+    b = P.rand_codes(g, (k, n))
+    sa = g.integers(120, 135, (m, 2), dtype=np.uint8)
+    sb = g.integers(120, 135, (n, 2), dtype=np.uint8)
+    out = oracle.k_grouped_fp8_gemm_tn_contiguous(a, F.pack_ue8m0(sa), b, F.pack_ue8m0(sb), [k])
+    # dense form needs block scales for B: use n <= 128 and per-row B scale equal across rows
+    sb_blk = np.tile(sb[:1], (n, 1))
+    out2 = oracle.k_grouped_fp8_gemm_tn_contiguous(a, F.pack_ue8m0(sa), b, F.pack_ue8m0(sb_blk), [k])
+    dense = oracle.fp8_gemm_nt(np.ascontiguousarray(a.T), F.pack_ue8m0(sa),
+                               np.ascontiguousarray(b.T), F.pack_ue8m0(sb[:1]))
+    assert np.array_equal(out2[0], dense)
+    assert out[0].shape == (m, n)
+
+
+# ------------------------------------------------------------------ mutants
+def _bias8_table():
+    t = F.E4M3_TABLE.copy()
+    t[np.isfinite(t)] /= 2
+    return t
+
+
+def _unsigned_table():
+    return np.abs(F.E4M3_TABLE)
+
+
+def _unpack_reversed(words, mn, groups):
+    w = np.asarray(words).view(np.uint32)
+    out = np.empty((mn, groups), dtype=np.uint8)
+    for g in range(groups):
+        out[:, g] = (w[g // 4, :mn] >> np.uint32(8 * (3 - g % 4))) & 0xFF
+    return out
+
+
+def _block_scales_mod(sfb_words, n, k):
+    blk = F.unpack_ue8m0(sfb_words, (n + 127) // 128, k // 128)
+    return blk[np.arange(n) % blk.shape[0]]
+
+
+def _dequant_no_scale(q, sf):
+    return F.e4m3_to_f64(q)
+
+
+_orig_nt = G.fp8_gemm_nt
+_orig_kg = G.k_grouped_fp8_gemm_tn_contiguous
+_orig_contig = G.m_grouped_fp8_gemm_nt_contiguous
+
+
+def _nt_drop_c(a, sfa, b, sfb, c=None, rows=None):
+    return _orig_nt(a, sfa, b, sfb, None, rows)
+
+
+def _nt_minus_c(a, sfa, b, sfb, c=None, rows=None):
+    d = _orig_nt(a, sfa, b, sfb, None, rows)
+    return d if c is None else d - np.asarray(c, np.float64)[rows if rows is not None else slice(None)]
+
+
+def _kg_shifted_offsets(a, sfa, b, sfb, ks, c=None, experts=None, rows=None):
+    ks = list(ks)
+    return _orig_kg(a, sfa, b, sfb, ks[1:] + ks[:1], c, experts, rows)
+
+
+def _contig_pad_as_expert0(a, sfa, b, sfb, m_indices, rows=None):
+    return _orig_contig(a, sfa, b, sfb, np.maximum(m_indices, 0), rows)
+
+
+def _row_scale_transposed(sfa_words, mn, k):
+    s = F.unpack_ue8m0(sfa_words, mn, k // 128)
+    return s[::-1]
+
+
+MUTANTS = {
+    "e4m3_bias_8": [(F, "E4M3_TABLE", _bias8_table)],
+    "e4m3_sign_dropped": [(F, "E4M3_TABLE", _unsigned_table)],
+    "scale_bytes_reversed": [(G, "unpack_ue8m0", lambda: _unpack_reversed)],
+    "b_block_index_mod": [(G, "block_scales", lambda: _block_scales_mod)],
+    "scale_dropped": [(G, "dequant_k_major", lambda: _dequant_no_scale)],
+    "c_dropped": [(G, "fp8_gemm_nt", lambda: _nt_drop_c)],
+    "c_sign_wrong": [(G, "fp8_gemm_nt", lambda: _nt_minus_c)],
+    "k_offsets_shifted": [(G, "k_grouped_fp8_gemm_tn_contiguous", lambda: _kg_shifted_offsets)],
+    "padding_rows_computed": [(G, "m_grouped_fp8_gemm_nt_contiguous", lambda: _contig_pad_as_expert0)],
+    "row_scales_wrong_row": [(G, "row_scales", lambda: _row_scale_transposed)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    for mod, attr, make in MUTANTS[name]:
+        monkeypatch.setattr(mod, attr, make())
+        # the package re-exports the GEMM entry points
+        if hasattr(oracle, attr):
+            monkeypatch.setattr(oracle, attr, getattr(mod, attr))
+    caught = []
+    for check in P.ALL_CHECKS:
+        try:
+            check()
+        except Exception:  # noqa: BLE001 - any failure counts as caught
+            caught.append(check.__name__)
+    assert caught, f"no pin detects mutant {name}"

@@ -1,0 +1,117 @@
+"""Seeded synthetic workloads for the fine-grained FP8 GEMM and its MoE variants.
+
+This module only draws random numbers and builds index structure (routing,
+segment lengths, masks, padding garbage).  It holds none of the GEMM's arithmetic:
+no FP8 or UE8M0 encoding, no scaling, no products.  The tests hand its draws to the
+oracle's quantiser; the benchmark hands them to the library's own quantise kernels.
+
+Every draw comes from ``numpy.random.Generator(PCG64(seed))`` so the same seed gives
+the same data on x86 and on Arm.
+
+Workloads (shapes and distributions of the five benchmark cases):
+
+* dense:      A[M,K], B[N,K] ~ N(0,1); optional C[M,N] ~ N(0,1).
+* contiguous: 8192 tokens x[T,K] ~ N(0,1); uniform logits over 256 experts, top-6;
+              the rows routed to experts 0..G-1 are kept, grouped by expert in
+              expert order, tokens ascending, each segment padded to a multiple of
+              128 rows marked -1 (garbage bytes); B[G,N,K] ~ N(0, 0.02).
+* masked:     G experts x M_max rows; valid rows x ~ N(0,1), masked_m[g] ~ U{0..M_max};
+              rows at or beyond the mask hold random bytes (NaN codes included) and
+              random scale bytes; B[G,N,K] ~ N(0, 0.02).
+* k-grouped:  per-expert K lengths ~ Multinomial(K_sum, uniform), each padded up to a
+              multiple of 128 with zero rows; A[K,M], B[K,N] ~ N(0,1); C[G,M,N] ~ N(0,1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ALIGN = 128
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _normal(g: np.random.Generator, shape, std=1.0) -> np.ndarray:
+    x = g.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def dense(seed: int, m: int, n: int, k: int, with_c: bool) -> dict:
+    g = rng(seed)
+    out = {"a": _normal(g, (m, k)), "b": _normal(g, (n, k)), "c": None}
+    if with_c:
+        out["c"] = _normal(g, (m, n))
+    return out
+
+
+def contiguous(seed: int, num_tokens: int = 8192, num_routed: int = 256, topk: int = 6,
+               num_groups: int = 32, n: int = 4096, k: int = 4096, b_std: float = 0.02) -> dict:
+    """Routing structure and draws for the M-grouped contiguous layout.
+
+    Returns x (token activations), ``row_token`` (token index of each valid row, or -1),
+    ``m_indices`` (expert of each row, -1 for padding), per-expert ``counts``,
+    ``garbage`` bytes and scale bytes for padding rows, and the expert weights ``b``."""
+    g = rng(seed)
+    x = _normal(g, (num_tokens, k))
+    logits = g.random((num_tokens, num_routed), dtype=np.float32)
+    top = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
+    m_indices, row_token, counts = [], [], []
+    for e in range(num_groups):
+        toks = np.nonzero((top == e).any(axis=1))[0]
+        counts.append(len(toks))
+        pad = (-len(toks)) % ALIGN
+        m_indices += [e] * len(toks) + [-1] * pad
+        row_token += list(toks) + [-1] * pad
+    m_total = len(m_indices)
+    return {
+        "x": x,
+        "m_indices": np.array(m_indices, dtype=np.int32),
+        "row_token": np.array(row_token, dtype=np.int64),
+        "counts": np.array(counts, dtype=np.int64),
+        "garbage": g.integers(0, 256, (m_total, k), dtype=np.uint8),
+        "garbage_sf": g.integers(0, 256, (m_total, k // ALIGN), dtype=np.uint8),
+        "b": _normal(g, (num_groups, n, k), b_std),
+    }
+
+
+def masked(seed: int, num_groups: int = 32, m_max: int = 256, n: int = 4096, k: int = 2048,
+           b_std: float = 0.02, masked_m=None) -> dict:
+    g = rng(seed)
+    if masked_m is None:
+        masked_m = g.integers(0, m_max + 1, num_groups)
+    masked_m = np.asarray(masked_m, dtype=np.int32)
+    return {
+        "x": _normal(g, (num_groups, m_max, k)),
+        "masked_m": masked_m,
+        "garbage": g.integers(0, 256, (num_groups, m_max, k), dtype=np.uint8),
+        "garbage_sf": g.integers(0, 256, (num_groups, m_max, k // ALIGN), dtype=np.uint8),
+        "b": _normal(g, (num_groups, n, k), b_std),
+    }
+
+
+def k_grouped(seed: int, num_groups: int = 8, m: int = 4096, n: int = 2048,
+              k_sum: int = 16384, ks=None) -> dict:
+    """Per-expert K lengths and draws for the K-grouped weight-gradient GEMM.
+    ``ks_true`` are the multinomial counts, ``ks`` the lengths padded to 128; the
+    padding rows of A and B are zero."""
+    g = rng(seed)
+    if ks is None:
+        ks_true = g.multinomial(k_sum, [1.0 / num_groups] * num_groups)
+    else:
+        ks_true = np.asarray(ks)
+    ks_true = np.asarray(ks_true, dtype=np.int64)
+    ks_pad = (ks_true + ALIGN - 1) // ALIGN * ALIGN
+    k_total = int(ks_pad.sum())
+    a = np.zeros((k_total, m), dtype=np.float32)
+    b = np.zeros((k_total, n), dtype=np.float32)
+    off = 0
+    for e in range(num_groups):
+        t = int(ks_true[e])
+        a[off:off + t] = _normal(g, (t, m))
+        b[off:off + t] = _normal(g, (t, n))
+        off += int(ks_pad[e])
+    return {"a": a, "b": b, "ks": ks_pad.astype(np.int32), "ks_true": ks_true,
+            "c": _normal(g, (num_groups, m, n))}
