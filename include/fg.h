@@ -1,0 +1,184 @@
+/*
+ * fg.h - C ABI of the fine-grained-scaled FP8 (E4M3) GEMM library for sm_103a.
+ *
+ * What the library computes is stated on the DeepGEMM pages:
+ *   - "DeepGEMM Documentation" (docsearch index), section 4 "Understand DeepGEMM GEMM
+ *     Naming and Layouts": D = C + A @ B; NT means non-transposed A, transposed B, so
+ *     fp8_gemm_nt computes D = C + A @ B.T; SM100 scaling factors are packed UE8M0,
+ *     four per 32-bit integer, and the LHS scaling factors are TMA-aligned and
+ *     transposed (MN-major).
+ *   - same page, section 9 "Use Normal and Grouped GEMM Kernels", and the
+ *     yuguo-Jack/DeepGEMM README, "Interfaces > Notices", "Grouped GEMMs (contiguous
+ *     layout)" and "Grouped GEMMs (masked layout)": the M-grouped contiguous, the
+ *     M-grouped masked and the K-grouped (weight-gradient, TN) variants.
+ *   - same page, section 10 "Use DeepGEMM Utility Functions": set/get_num_sms,
+ *     get_mk_alignment_for_contiguous_layout, get_tma_aligned_size.
+ *
+ * Conventions shared by every GEMM entry point
+ *   - All array arguments are DEVICE pointers owned by the caller; the library never
+ *     frees, keeps or allocates them, and allocates nothing per call.
+ *   - FP8 operands are E4M3 bytes (OCP "fn": bias 7, no inf, S.1111.111 = NaN).
+ *   - Scale factors are UE8M0 (value 2^(u-127)), packed four per int32: byte j
+ *     (bits 8j..8j+7) of word w is the scale of K-group 4w+j, a K-group being 128
+ *     consecutive K elements.  Packed scale arrays are MN-major:
+ *     [ceil(K/512)][align4(MN)] int32, with align4(x) = x rounded up to a multiple
+ *     of 4 (16 bytes).  Padding entries are ignored.
+ *   - A scales are one per row per K-group (1x128).  B scales of the NT calls are
+ *     one per 128x128 block (MN index = n / 128); the K-grouped call takes 1x128
+ *     scales along K for both operands.
+ *   - C is optional FP32 and is accepted only with an FP32 D; D may alias C.
+ *     A BF16 D is round-to-nearest-even of the FP32 accumulator.
+ *   - Alignment: A, B, C, D and the scale arrays must be 16-byte aligned;
+ *     index arrays 4-byte aligned.  K (or every K segment) is a multiple of 128,
+ *     N a multiple of 16.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 is the legacy default
+ *     stream): no host synchronisation, no allocation.  The current CUDA device must
+ *     own all pointers.
+ *   - Return value: FG_OK, or a negative fg_status.  Host-side argument errors return
+ *     FG_ERR_INVALID_ARG / FG_ERR_UNSUPPORTED before anything is launched.  A launch
+ *     failure returns FG_ERR_CUDA.  Contract violations found on the device (index or
+ *     mask out of range, bad K segments) and internal wait time-outs never trap: the
+ *     kernel skips the offending tile (or the whole call), records the first such
+ *     event in a per-device status word and returns; fg_get_device_error reads it.
+ *   - Results are deterministic: no atomics touch D, no split-K.
+ */
+#ifndef FG_H
+#define FG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so a cudaStream_t (or torch's stream handle) passes as is. */
+typedef struct CUstream_st* fg_stream_t;
+
+typedef enum {
+    FG_OK = 0,
+    FG_ERR_INVALID_ARG = -1,       /* null/misaligned pointer, bad shape or dtype code */
+    FG_ERR_UNSUPPORTED = -2,       /* valid but not provided (e.g. C with a BF16 D)    */
+    FG_ERR_CUDA = -3,              /* a CUDA runtime/driver call failed (no device...)  */
+    FG_ERR_DEVICE_CONTRACT = -4,   /* device-side index/mask/segment contract violated  */
+    FG_ERR_DEVICE_TIMEOUT = -5     /* a bounded wait inside a kernel ran out            */
+} fg_status;
+
+typedef enum { FG_BF16 = 0, FG_F32 = 1 } fg_dtype;
+
+/*
+ * Dense NT GEMM:  D[M,N] = C[M,N] + A[M,K] @ B[N,K]^T, with the fine-grained scales
+ * applied per K-group (docsearch section 4; README "Interfaces > Notices").
+ *   a    [M][K]   E4M3, row-major (K contiguous)
+ *   sfa  [ceil(K/512)][align4(M)] packed UE8M0, one scale per row per K-group
+ *   b    [N][K]   E4M3, row-major (K contiguous)
+ *   sfb  [ceil(K/512)][align4(ceil(N/128))] packed UE8M0, one scale per 128x128 block
+ *   c    [M][N]   FP32 or NULL; needs d_dtype == FG_F32; may equal d
+ *   d    [M][N]   BF16 or FP32 (d_dtype)
+ * M >= 0 (M == 0 returns FG_OK), K >= 128 and K % 128 == 0, N >= 16 and N % 16 == 0.
+ */
+int fg_fp8_gemm_nt(int M, int N, int K,
+                   const uint8_t* a, const int32_t* sfa,
+                   const uint8_t* b, const int32_t* sfb,
+                   const float* c, void* d, int d_dtype, fg_stream_t stream);
+
+/*
+ * M-grouped contiguous NT GEMM (docsearch section 9 item 2; README "Grouped GEMMs
+ * (contiguous layout)"): the token rows of all groups (experts) are concatenated
+ * along M, every group segment aligned to fg_get_mk_alignment_for_contiguous_layout()
+ * rows.  Row m uses the weights of group m_indices[m]:
+ *   D[m,:] = A[m,:] @ B[m_indices[m]]^T
+ *   a          [M_total][K] E4M3;  sfa [ceil(K/512)][align4(M_total)]
+ *   b          [G][N][K]    E4M3;  sfb [G][ceil(K/512)][align4(ceil(N/128))]
+ *   m_indices  [M_total] int32 on the device: group id in [0,G), or -1 for padding
+ *   d          [M_total][N] BF16 or FP32
+ * Rows with m_indices == -1 are neither computed into D nor written.  Within each
+ * 128-row block all non-padding rows must name one group; a block whose first row is
+ * -1 is skipped.  A row naming another group, or a group id >= G, is a device
+ * contract violation: that row (or block) is left unwritten and the status word is set.
+ * M_total % 128 == 0, G >= 1.  No C operand.
+ */
+int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G,
+                                        const uint8_t* a, const int32_t* sfa,
+                                        const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* m_indices,
+                                        void* d, int d_dtype, fg_stream_t stream);
+
+/*
+ * M-grouped masked NT GEMM (docsearch section 9 item 4; README "Grouped GEMMs (masked
+ * layout)"): group g owns rows [0, M_max) of its slice; only rows m < masked_m[g]
+ * are valid.  The counts live on the device, so the call needs no host knowledge of
+ * them and can sit inside a CUDA graph:
+ *   D[g, m, :] = A[g, m, :] @ B[g]^T        for m < masked_m[g]
+ *   a         [G][M_max][K] E4M3;  sfa [G][ceil(K/512)][align4(M_max)]
+ *   b         [G][N][K]     E4M3;  sfb [G][ceil(K/512)][align4(ceil(N/128))]
+ *   masked_m  [G] int32 on the device, each in [0, M_max]
+ *   expected_m  host hint of the typical masked_m (tile-size choice only; <= 0: none);
+ *               results never depend on it
+ *   d         [G][M_max][N] BF16 or FP32
+ * Rows m >= masked_m[g] are never written, and their A rows (which may hold any bytes,
+ * NaN codes included) never reach a valid row.  A mask outside [0, M_max] is clamped
+ * and recorded as a device contract violation.  G >= 1, M_max >= 1.  No C operand.
+ */
+int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K,
+                                    const uint8_t* a, const int32_t* sfa,
+                                    const uint8_t* b, const int32_t* sfb,
+                                    const int32_t* masked_m, int expected_m,
+                                    void* d, int d_dtype, fg_stream_t stream);
+
+/*
+ * K-grouped contiguous TN GEMM, the MoE weight gradient (docsearch section 9 item 3;
+ * README "Grouped GEMMs (contiguous layout)", last paragraph): M and N are fixed,
+ * and group g owns the K rows [off_g, off_g + ks[g]) of both operands:
+ *   D[g] = C[g] + A[off_g : off_g+ks[g], :]^T @ B[off_g : off_g+ks[g], :]
+ *   a    [K_total][M] E4M3 (M contiguous: MN-major)
+ *   sfa  [ceil(K_total/512)][align4(M)] packed UE8M0, 1x128 along K per column m
+ *   b    [K_total][N] E4M3 (N contiguous)
+ *   sfb  [ceil(K_total/512)][align4(N)] packed UE8M0, 1x128 along K per column n
+ *   ks   [G] int32 on the device; each a multiple of 128 (0 allowed); sum == K_total
+ *   c    [G][M][N] FP32 or NULL (NULL: C = 0); may equal d
+ *   d    [G][M][N] FP32
+ * Scale groups are counted over the concatenated K axis (group of element k is k/128),
+ * so no group straddles two segments.  A ks that breaks these rules is a device
+ * contract violation: nothing is written and the status word is set.
+ * G >= 1, M >= 1, K_total % 128 == 0, M % 16 == 0, N % 16 == 0.
+ */
+int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total,
+                                        const uint8_t* a, const int32_t* sfa,
+                                        const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* ks, const float* c, float* d,
+                                        fg_stream_t stream);
+
+/* Row alignment of each group segment in the contiguous layout: 128, the M block
+ * (docsearch section 9 item 2 and section 10). */
+int fg_get_mk_alignment_for_contiguous_layout(void);
+
+/* x rounded up so that x * elem_bytes is a multiple of 16 bytes (section 10,
+ * get_tma_aligned_size).  Returns -1 for elem_bytes not in {1,2,4,8} or x < 0. */
+int fg_get_tma_aligned_size(int x, int elem_bytes);
+
+/* Maximum number of SMs the persistent kernels use (section 10, set/get_num_sms).
+ * n <= 0 restores the default (all SMs of the current device).  get returns the value
+ * in force for the current device, or -1 when no device is available. */
+void fg_set_num_sms(int n);
+int fg_get_num_sms(void);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: FG_OK, FG_ERR_DEVICE_CONTRACT or FG_ERR_DEVICE_TIMEOUT (first event
+ * since the last read), or FG_ERR_CUDA if the synchronisation itself failed.
+ * *detail (may be NULL) receives the raw code: which check fired and where. */
+int fg_get_device_error(fg_stream_t stream, int* detail);
+
+/* Static description of a status code. */
+const char* fg_status_string(int status);
+
+/* Test hook for the time-out path: while enabled, the next GEMM launches have their
+ * operand producer skip its first stage, so the MMA issuer's bounded wait runs out
+ * after timeout_us microseconds, the kernel records FG_ERR_DEVICE_TIMEOUT and every
+ * role exits cleanly.  enable = 0 restores normal operation and the default time-out. */
+void fg_debug_inject_stall(int enable, uint32_t timeout_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FG_H */

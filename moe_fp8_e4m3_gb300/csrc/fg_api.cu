@@ -1,0 +1,391 @@
+// fg_api.cu - the C ABI declared in include/fg.h: host-side validation, TMA tensor-map
+// encoding, tile-size choice and launch of the persistent FP8 GEMM kernels.
+//
+// No allocation happens per call.  Per device the library keeps the SM count and the
+// device address of its status word; the TMA encoder is fetched once from the driver.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fg.h"
+#include "fg_launch.h"
+
+// Device status word: first contract violation or wait time-out since the last read.
+__device__ int g_fg_status = 0;
+
+namespace {
+
+using fg::GemmParams;
+
+constexpr int kMaxDevices = 256;
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_num_sms_limit = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+int g_debug_stall = 0;
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FG_ERR_CUDA;
+        }
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_fg_status) != cudaSuccess) {
+            cudaGetLastError();
+            return FG_ERR_CUDA;
+        }
+        st.num_sms = sms;
+        st.status = static_cast<int*>(ptr);
+        st.ready = true;
+    }
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        cudaDriverEntryPointQueryResult q{};
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    }
+    if (!g_encode) return FG_ERR_CUDA;
+    *out = &st;
+    return FG_OK;
+}
+
+int sms_in_use(const DeviceState& st) {
+    return (g_num_sms_limit > 0 && g_num_sms_limit < st.num_sms) ? g_num_sms_limit : st.num_sms;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+int align4(int x) { return (x + 3) / 4 * 4; }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// 2-D tiled tensor map over a row-major [outer][inner] array with the given row pitch.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box,
+                                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool print_configs() {
+    const char* e = std::getenv("FG_PRINT_CONFIGS");
+    return e && e[0] == '1';
+}
+
+// Optional override of the N tile (tuning aid): FG_FORCE_BN=64|128|256.
+int forced_bn() {
+    const char* e = std::getenv("FG_FORCE_BN");
+    return e ? std::atoi(e) : 0;
+}
+
+// N-tile choice: the widest tile that still gives every SM at least one tile; narrower
+// tiles when the problem has too few row blocks to fill the GPU.
+int choose_bn_nt(long long row_blocks, int n, int sms) {
+    const int f = forced_bn();
+    if (f == 64 || f == 128 || f == 256) return f;
+    for (int bn : {256, 128}) {
+        if (row_blocks * ceil_div(n, bn) >= sms) return bn;
+    }
+    return 64;
+}
+
+int choose_bn_tn(long long row_blocks, int n, int sms) {
+    const int f = forced_bn();
+    if (f == 128 || f == 256) return f;
+    return row_blocks * ceil_div(n, 256) >= sms ? 256 : 128;
+}
+
+void fill_common(GemmParams& p, const DeviceState& st) {
+    p.status = st.status;
+    p.timeout_ns = g_timeout_ns;
+    p.debug_stall = g_debug_stall;
+}
+
+int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
+              cudaStream_t s) {
+    cudaError_t e;
+    switch (bn) {
+        case 64: e = fg::launch_gemm<64, false>(p, ma, mb, grid, s); break;
+        case 128: e = fg::launch_gemm<128, false>(p, ma, mb, grid, s); break;
+        default: e = fg::launch_gemm<256, false>(p, ma, mb, grid, s); break;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    return FG_OK;
+}
+
+int launch_tn(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
+              cudaStream_t s) {
+    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, ma, mb, grid, s)
+                                    : fg::launch_gemm<256, true>(p, ma, mb, grid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    return FG_OK;
+}
+
+// Shared checks of the NT operands: FP8 A/B and the packed scale arrays.
+int check_nt_operands(int n, int k, const void* a, const void* sfa, const void* b,
+                      const void* sfb, const void* d, int d_dtype) {
+    if (n < 16 || n % 16 != 0 || k < 128 || k % 128 != 0) return FG_ERR_INVALID_ARG;
+    if (d_dtype != FG_BF16 && d_dtype != FG_F32) return FG_ERR_INVALID_ARG;
+    if (!a || !sfa || !b || !sfb || !d) return FG_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d))
+        return FG_ERR_INVALID_ARG;
+    return FG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    if (M < 0) return FG_ERR_INVALID_ARG;
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    if (rc) return rc;
+    if (c && !aligned16(c)) return FG_ERR_INVALID_ARG;
+    if (c && d_dtype != FG_F32) return FG_ERR_UNSUPPORTED;
+    if (M == 0) return FG_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    const int num_mb = ceil_div(M, 128);
+    const int bn = choose_bn_nt(num_mb, N, sms);
+    GemmParams p{};
+    p.kind = fg::kDense;
+    p.M = M; p.N = N; p.K = K; p.G = 1;
+    p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
+    p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
+    p.sfa = sfa; p.sfb = sfb;
+    p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_rows = M;
+    p.c = c; p.d = d;
+    fill_common(p, *st);
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FG_ERR_INVALID_ARG;
+    const long long tiles = (long long)p.num_mb * p.num_nb;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (print_configs())
+        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d tiles=%lld grid=%d\n", M, N, K, bn, tiles, grid);
+    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
+                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* m_indices, void* d, int d_dtype,
+                                        fg_stream_t stream) {
+    if (M_total < 0 || M_total % 128 != 0 || G < 1) return FG_ERR_INVALID_ARG;
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    if (rc) return rc;
+    if (!m_indices || !aligned4(m_indices)) return FG_ERR_INVALID_ARG;
+    if ((long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
+    if (M_total == 0) return FG_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    const int num_mb = M_total / 128;
+    const int bn = choose_bn_nt(num_mb, N, sms);
+    GemmParams p{};
+    p.kind = fg::kContiguous;
+    p.M = M_total; p.N = N; p.K = K; p.G = G;
+    p.d_f32 = d_dtype == FG_F32; p.has_c = 0;
+    p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
+    p.sfa = sfa; p.sfb = sfb;
+    p.sfa_ld = align4(M_total); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    p.sfa_rows = M_total;
+    p.m_indices = m_indices;
+    p.d = d;
+    fill_common(p, *st);
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FG_ERR_INVALID_ARG;
+    const long long tiles = (long long)p.num_mb * p.num_nb;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (print_configs())
+        std::fprintf(stderr, "[fg] m_grouped_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
+                     M_total, N, K, G, bn, grid);
+    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
+                                    const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                    const int32_t* masked_m, int expected_m, void* d, int d_dtype,
+                                    fg_stream_t stream) {
+    if (G < 1 || G > fg::kMaxGroups || M_max < 1) return FG_ERR_INVALID_ARG;
+    if ((long long)G * M_max > 0x7fffffffLL || (long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    if (rc) return rc;
+    if (!masked_m || !aligned4(masked_m)) return FG_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    const int hint = expected_m > 0 ? (expected_m < M_max ? expected_m : M_max) : M_max;
+    const int bn = choose_bn_nt((long long)G * ceil_div(hint, 128), N, sms);
+    GemmParams p{};
+    p.kind = fg::kMasked;
+    p.M = M_max; p.N = N; p.K = K; p.G = G;
+    p.d_f32 = d_dtype == FG_F32; p.has_c = 0;
+    p.num_mb = ceil_div(M_max, 128); p.num_nb = ceil_div(N, bn);
+    p.sfa = sfa; p.sfb = sfb;
+    p.sfa_ld = align4(M_max); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_gstride = (long long)ceil_div(K, 512) * p.sfa_ld;
+    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    p.sfa_rows = M_max;
+    p.masked_m = masked_m;
+    p.d = d;
+    fill_common(p, *st);
+    CUtensorMap ma, mb;
+    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FG_ERR_INVALID_ARG;
+    const long long tiles = (long long)G * p.num_mb * p.num_nb;   // upper bound
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (print_configs())
+        std::fprintf(stderr, "[fg] m_grouped_masked G=%d M_max=%d N=%d K=%d BN=%d grid=%d\n", G, M_max, N, K, bn, grid);
+    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const uint8_t* a,
+                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* ks, const float* c, float* d,
+                                        fg_stream_t stream) {
+    if (G < 1 || G > fg::kMaxGroups || M < 16 || M % 16 != 0 || N < 16 || N % 16 != 0 ||
+        K_total < 0 || K_total % 128 != 0)
+        return FG_ERR_INVALID_ARG;
+    if ((long long)G * M > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
+    if (!ks || !aligned4(ks) || !d || !aligned16(d) || (c && !aligned16(c))) return FG_ERR_INVALID_ARG;
+    if (K_total > 0 && (!a || !sfa || !b || !sfb || !aligned16(a) || !aligned16(sfa) ||
+                        !aligned16(b) || !aligned16(sfb)))
+        return FG_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    const int num_mb = ceil_div(M, 128);
+    const int bn = choose_bn_tn((long long)G * num_mb, N, sms);
+    GemmParams p{};
+    p.kind = fg::kKGrouped;
+    p.M = M; p.N = N; p.K = K_total; p.G = G;
+    p.d_f32 = 1; p.has_c = c != nullptr;
+    p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
+    p.sfa = sfa; p.sfb = sfb;
+    p.sfa_ld = align4(M); p.sfb_ld = align4(N);
+    p.sfa_rows = M;
+    p.ks = ks;
+    p.c = c; p.d = d;
+    fill_common(p, *st);
+    CUtensorMap ma, mb;
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    // With K_total == 0 every segment is empty and no operand load is ever issued.
+    if (K_total > 0 &&
+        (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K_total, M, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, K_total, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return FG_ERR_INVALID_ARG;
+    const long long tiles = (long long)G * p.num_mb * p.num_nb;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (print_configs())
+        std::fprintf(stderr, "[fg] k_grouped_tn G=%d M=%d N=%d K_total=%d BN=%d grid=%d\n", G, M, N, K_total, bn, grid);
+    return launch_tn(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fg_get_mk_alignment_for_contiguous_layout(void) { return 128; }
+
+int fg_get_tma_aligned_size(int x, int elem_bytes) {
+    if (x < 0 || (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)) return -1;
+    const int per = 16 / elem_bytes;
+    return (x + per - 1) / per * per;
+}
+
+void fg_set_num_sms(int n) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_num_sms_limit = n > 0 ? n : 0;
+}
+
+int fg_get_num_sms(void) {
+    DeviceState* st = nullptr;
+    if (device_state(&st)) return -1;
+    return sms_in_use(*st);
+}
+
+int fg_get_device_error(fg_stream_t stream, int* detail) {
+    if (detail) *detail = 0;
+    DeviceState* st = nullptr;
+    if (device_state(&st)) return FG_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    if (detail) *detail = v;
+    if (v == 0) return FG_OK;
+    if (v & fg::kErrTimeout) return FG_ERR_DEVICE_TIMEOUT;
+    return FG_ERR_DEVICE_CONTRACT;
+}
+
+const char* fg_status_string(int status) {
+    switch (status) {
+        case FG_OK: return "ok";
+        case FG_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, bad shape or dtype)";
+        case FG_ERR_UNSUPPORTED: return "unsupported combination (e.g. C with a BF16 D)";
+        case FG_ERR_CUDA: return "CUDA runtime or driver call failed";
+        case FG_ERR_DEVICE_CONTRACT: return "device-side contract violation (indices, mask or K segments)";
+        case FG_ERR_DEVICE_TIMEOUT: return "bounded wait inside a kernel timed out";
+        default: return "unknown status";
+    }
+}
+
+void fg_debug_inject_stall(int enable, uint32_t timeout_us) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_debug_stall = enable ? 1 : 0;
+    g_timeout_ns = enable && timeout_us > 0 ? 1000ull * timeout_us : kDefaultTimeoutNs;
+}
+
+}  // extern "C"

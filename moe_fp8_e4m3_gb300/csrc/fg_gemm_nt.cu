@@ -1,0 +1,9 @@
+// fg_gemm_nt.cu - NT (K-major A and B) kernel variants: dense, M-grouped contiguous and
+// M-grouped masked GEMMs.
+#include "fg_gemm_inst.cuh"
+
+namespace fg {
+template cudaError_t launch_gemm<64, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<128, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+}  // namespace fg

@@ -1,0 +1,7 @@
+// fg_gemm_tn.cu - TN (MN-major A and B) kernel variants: the K-grouped weight-gradient GEMM.
+#include "fg_gemm_inst.cuh"
+
+namespace fg {
+template cudaError_t launch_gemm<128, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+}  // namespace fg

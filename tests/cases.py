@@ -1,0 +1,127 @@
+"""Test cases for the GPU parity tests: seeded draws from ``workloads`` encoded by the
+oracle's quantiser, the oracle's expected values, and the comparison rule.
+
+Tolerance (the stated accuracy target of the FP8 GEMM): per element
+|d - ref| <= 1e-2 * |ref| + 1e-2 * rms(ref), and the normalised difference
+1 - 2<x,y> / (|x|^2 + |y|^2) <= 1e-5, both over the valid rows only."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads
+from oracle import formats as F
+
+REL_TOL = 1e-2
+DIFF_TOL = 1e-5
+SENTINEL_BF16 = 0x7FBF
+SENTINEL_F32 = 0x7FBFFFFF
+
+
+def compare(got: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
+    got = np.asarray(got, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    if ref.size == 0:
+        return {"n": 0}
+    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = np.abs(got - ref)
+    bound = REL_TOL * np.abs(ref) + REL_TOL * rms
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), (f"{what}: element {worst} got {got[worst]} ref {ref[worst]} "
+                                  f"(bound {bound[worst]:.3g}); {int((err > bound).sum())} bad of {ref.size}")
+    denom = float(np.dot(got, got) + np.dot(ref, ref))
+    diff = 0.0 if denom == 0 else 1.0 - 2.0 * float(np.dot(got, ref)) / denom
+    assert diff <= DIFF_TOL, f"{what}: normalised difference {diff:.3g} > {DIFF_TOL}"
+    return {"n": ref.size, "max_rel_to_rms": float(err.max() / max(rms, 1e-300)), "diff": diff}
+
+
+# ------------------------------------------------------------------ dense
+def dense_case(seed, m, n, k, with_c, out="bf16"):
+    w = workloads.dense(seed, m, n, k, with_c)
+    a, sa = F.quantize_rows(w["a"])
+    b, sb = F.quantize_blocks(w["b"])
+    return {"m": m, "n": n, "k": k, "a": a, "sfa": F.pack_ue8m0(sa), "b": b, "sfb": F.pack_ue8m0(sb),
+            "c": w["c"], "out": out}
+
+
+def dense_ref(case, rows=None):
+    return oracle.fp8_gemm_nt(case["a"], case["sfa"], case["b"], case["sfb"], case["c"], rows=rows)
+
+
+# ------------------------------------------------------------- contiguous
+def contiguous_case(seed, **kw):
+    w = workloads.contiguous(seed, **kw)
+    m_indices = w["m_indices"]
+    m_total = len(m_indices)
+    k = w["x"].shape[1]
+    valid = w["row_token"] >= 0
+    a = w["garbage"].copy()
+    sa = w["garbage_sf"].copy()
+    qa, qsa = F.quantize_rows(w["x"][w["row_token"][valid]])
+    a[valid] = qa
+    sa[valid] = qsa
+    g_count, n, _ = w["b"].shape
+    bq = np.empty((g_count, n, k), np.uint8)
+    sfb = []
+    for e in range(g_count):
+        bq[e], sb = F.quantize_blocks(w["b"][e])
+        sfb.append(F.pack_ue8m0(sb))
+    return {"m_total": m_total, "n": n, "k": k, "g": g_count, "a": a, "sfa": F.pack_ue8m0(sa),
+            "b": bq, "sfb": np.stack(sfb), "m_indices": m_indices, "counts": w["counts"]}
+
+
+def contiguous_ref(case, rows=None):
+    return oracle.m_grouped_fp8_gemm_nt_contiguous(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                   case["m_indices"], rows=rows)
+
+
+# ----------------------------------------------------------------- masked
+def masked_case(seed, **kw):
+    w = workloads.masked(seed, **kw)
+    g_count, m_max, k = w["x"].shape
+    n = w["b"].shape[1]
+    a = w["garbage"].copy()
+    sfa = []
+    bq = np.empty((g_count, n, k), np.uint8)
+    sfb = []
+    for e in range(g_count):
+        mm = int(w["masked_m"][e])
+        sa = w["garbage_sf"][e].copy()
+        if mm > 0:
+            qa, qsa = F.quantize_rows(w["x"][e, :mm])
+            a[e, :mm] = qa
+            sa[:mm] = qsa
+        sfa.append(F.pack_ue8m0(sa))
+        bq[e], sb = F.quantize_blocks(w["b"][e])
+        sfb.append(F.pack_ue8m0(sb))
+    return {"g": g_count, "m_max": m_max, "n": n, "k": k, "a": a, "sfa": np.stack(sfa), "b": bq,
+            "sfb": np.stack(sfb), "masked_m": w["masked_m"]}
+
+
+def masked_ref(case, experts=None):
+    return oracle.m_grouped_fp8_gemm_nt_masked(case["a"], case["sfa"], case["b"], case["sfb"],
+                                               case["masked_m"], experts=experts)
+
+
+# -------------------------------------------------------------- K-grouped
+def k_grouped_case(seed, with_c=True, **kw):
+    w = workloads.k_grouped(seed, **kw)
+    a, sa = F.quantize_cols(w["a"])
+    b, sb = F.quantize_cols(w["b"])
+    return {"g": len(w["ks"]), "m": w["a"].shape[1], "n": w["b"].shape[1], "k_total": w["a"].shape[0],
+            "a": a, "sfa": F.pack_ue8m0(sa), "b": b, "sfb": F.pack_ue8m0(sb), "ks": w["ks"],
+            "c": w["c"] if with_c else None}
+
+
+def k_grouped_ref(case, experts=None, rows=None):
+    return oracle.k_grouped_fp8_gemm_tn_contiguous(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                   case["ks"], case["c"], experts=experts, rows=rows)
+
+
+def decode_out(arr: np.ndarray, out: str) -> np.ndarray:
+    """GPU output (bf16 bits as uint16/int16, or float32) to float64."""
+    if out == "bf16":
+        return F.bf16_to_f64(arr.view(np.uint16))
+    return arr.astype(np.float64)

@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA library (through the C ABI) against the oracle, element by
+element on the same seeded inputs, plus bit-exact probes and untouched-row checks."""
+import numpy as np
+import pytest
+
+import cases as C
+import oracle_pins as P
+from oracle import formats as F
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import moe_fp8_e4m3_gb300 as lib
+    return lib
+
+
+def _status_ok(fg):
+    st, detail = fg.get_device_error()
+    assert st == 0, (st, hex(detail))
+
+
+def run_dense(fg, case, alias_c=False):
+    from gpu_util import GuardedOut, dev
+    out = GuardedOut(case["m"], case["n"], case["out"])
+    c_t = None
+    if case["c"] is not None:
+        if alias_c:
+            out.fill_from(case["c"])
+            c_t = out.tensor
+        else:
+            c_t = dev(case["c"])
+    fg.fp8_gemm_nt(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), out.tensor, c=c_t)
+    _status_ok(fg)
+    out.check_guards()
+    return out
+
+
+# ------------------------------------------------------------------ dense
+@pytest.mark.parametrize("m,n,k,with_c,out", [
+    (128, 256, 512, False, "bf16"),       # the small dense case
+    (200, 272, 384, True, "f32"),         # ragged M and N tails, C
+    (1, 16, 128, False, "bf16"),          # minimum sizes
+    (64, 512, 1024, True, "f32"),         # decode-like M
+    (300, 1000 // 16 * 16, 640, False, "bf16"),
+    (513, 384, 2560, True, "f32"),        # K spans several packed scale words
+])
+def test_dense_parity(fg, m, n, k, with_c, out):
+    case = C.dense_case(100 + m + n + k, m, n, k, with_c, out)
+    got = run_dense(fg, case)
+    C.compare(got.values(), C.dense_ref(case), f"dense {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("bn", ["64", "128", "256"])
+def test_dense_every_tile_width(fg, bn, monkeypatch):
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.dense_case(7, 256, 768, 512, True, "f32")
+    got = run_dense(fg, case)
+    C.compare(got.values(), C.dense_ref(case), f"BN={bn}")
+
+
+def test_dense_d_aliases_c(fg):
+    case = C.dense_case(8, 256, 256, 256, True, "f32")
+    got = run_dense(fg, case, alias_c=True)
+    C.compare(got.values(), C.dense_ref(case), "aliased C")
+
+
+def test_scale_identification_probe_bit_exact(fg):
+    """A = B = 1.0; every (row, group) and (n-block, group) scale is a distinct power of
+    two, so each FP32 output names exactly which scales were applied."""
+    from gpu_util import GuardedOut, dev
+    m, n, groups = 256, 512, 8
+    ea, eb = P.scale_probe_inputs(m, n, groups)
+    a = np.full((m, groups * 128), 0x38, np.uint8)
+    b = np.full((n, groups * 128), 0x38, np.uint8)
+    sfa = F.pack_ue8m0((ea + 127).astype(np.uint8))
+    sfb = F.pack_ue8m0((eb + 127).astype(np.uint8))
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_gemm_nt(dev(a), dev(sfa), dev(b), dev(sfb), out.tensor)
+    _status_ok(fg)
+    want = np.zeros((m, n))
+    for gg in range(groups):
+        want += 2.0 ** (7 + ea[:, gg][:, None] + eb[np.arange(n) // 128, gg][None, :])
+    got = out.values()
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:4].tolist()}: got {got[tuple(bad[0])]} want {want[tuple(bad[0])]}"
+
+
+def test_integer_valued_bit_exact(fg):
+    from gpu_util import GuardedOut, dev
+    g = np.random.Generator(np.random.PCG64(12))
+    codes = np.array([0xB8, 0x00, 0x38], np.uint8)          # -1, 0, 1
+    ai = g.integers(-1, 2, (160, 128))
+    bi = g.integers(-1, 2, (96, 128))
+    a, b = codes[ai + 1], codes[bi + 1]
+    sfa = F.pack_ue8m0(np.full((160, 1), 127, np.uint8))
+    sfb = F.pack_ue8m0(np.full((1, 1), 127, np.uint8))
+    out = GuardedOut(160, 96, "bf16")
+    fg.fp8_gemm_nt(dev(a), dev(sfa), dev(b), dev(sfb), out.tensor)
+    _status_ok(fg)
+    assert np.array_equal(out.values(), (ai @ bi.T).astype(np.float64))
+
+
+def test_identity_bit_exact(fg):
+    from gpu_util import GuardedOut, dev
+    g = np.random.Generator(np.random.PCG64(4))
+    a = np.zeros((128, 128), np.uint8)
+    np.fill_diagonal(a, 0x38)
+    b = P.rand_codes(g, (256, 128))
+    sfb_bytes = np.array([[121], [133]], np.uint8)
+    out = GuardedOut(128, 256, "bf16")
+    fg.fp8_gemm_nt(dev(a), dev(F.pack_ue8m0(np.full((128, 1), 127, np.uint8))), dev(b),
+                   dev(F.pack_ue8m0(sfb_bytes)), out.tensor)
+    _status_ok(fg)
+    want = (F.e4m3_to_f64(b) * F.ue8m0_to_f64(sfb_bytes[np.arange(256) // 128])).T
+    assert np.array_equal(out.values(), want)
+
+
+# ------------------------------------------------------------- contiguous
+def run_contiguous(fg, case, out="bf16"):
+    from gpu_util import GuardedOut, dev
+    d = GuardedOut(case["m_total"], case["n"], out)
+    fg.m_grouped_fp8_gemm_nt_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(case["m_indices"]), d.tensor)
+    _status_ok(fg)
+    d.check_guards()
+    return d
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_contiguous_parity(fg, out):
+    case = C.contiguous_case(2, num_tokens=512, num_routed=16, topk=3, num_groups=5, n=256, k=384)
+    d = run_contiguous(fg, case, out)
+    ref, written = C.contiguous_ref(case)
+    assert np.array_equal(~d.is_sentinel(), written), "written row set differs"
+    C.compare(d.values()[written], ref[written], "contiguous")
+
+
+def test_contiguous_empty_groups_and_all_padding_block(fg):
+    # group 1 receives no tokens; the last block is all padding
+    g = np.random.Generator(np.random.PCG64(31))
+    m_indices = np.array([0] * 130 + [-1] * 126 + [2] * 128 + [-1] * 128, np.int32)
+    k, n, groups = 256, 128, 3
+    a = P.rand_codes(g, (len(m_indices), k))
+    b = P.rand_codes(g, (groups, n, k))
+    sfa = P.rand_words(g, len(m_indices), k // 128)
+    sfb = np.stack([P.rand_words(g, 1, k // 128) for _ in range(groups)])
+    case = {"m_total": len(m_indices), "n": n, "k": k, "g": groups, "a": a, "sfa": sfa, "b": b,
+            "sfb": sfb, "m_indices": m_indices}
+    d = run_contiguous(fg, case)
+    ref, written = C.contiguous_ref(case)
+    assert np.array_equal(~d.is_sentinel(), written)
+    C.compare(d.values()[written], ref[written], "contiguous edge")
+
+
+def test_contiguous_contract_violation_reported(fg):
+    from gpu_util import GuardedOut, dev
+    g = np.random.Generator(np.random.PCG64(32))
+    m_indices = np.array([0] * 128 + [5] * 128, np.int32)   # group 5 >= G
+    k, n = 128, 64
+    a = P.rand_codes(g, (256, k))
+    b = P.rand_codes(g, (2, n, k))
+    d = GuardedOut(256, n, "bf16")
+    fg.m_grouped_fp8_gemm_nt_contiguous(dev(a), dev(P.rand_words(g, 256, 1)), dev(b),
+                                        dev(np.stack([P.rand_words(g, 1, 1)] * 2)), dev(m_indices), d.tensor)
+    st, detail = fg.get_device_error()
+    assert st == fg.FG_ERR_DEVICE_CONTRACT and detail == 0x101
+    assert np.all(d.is_sentinel()[128:]) and not np.any(d.is_sentinel()[:128])
+
+
+# ----------------------------------------------------------------- masked
+def run_masked(fg, case, out="bf16"):
+    from gpu_util import GuardedOut, dev
+    d = GuardedOut(case["g"] * case["m_max"], case["n"], out)
+    fg.m_grouped_fp8_gemm_nt_masked(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                    dev(case["masked_m"]), d.tensor.view(case["g"], case["m_max"], case["n"]))
+    _status_ok(fg)
+    d.check_guards()
+    return d
+
+
+def _check_masked(case, d):
+    ref = C.masked_ref(case)
+    vals = d.values().reshape(case["g"], case["m_max"], case["n"])
+    sent = d.is_sentinel().reshape(case["g"], case["m_max"])
+    for e in range(case["g"]):
+        mm = int(case["masked_m"][e])
+        assert not sent[e, :mm].any() and sent[e, mm:].all(), f"group {e}: rows beyond mask written"
+        if mm:
+            C.compare(vals[e, :mm], ref[e], f"masked group {e}")
+
+
+@pytest.mark.parametrize("masks", [[0, 1, 192, 100], [128, 129, 64, 0]])
+def test_masked_parity(fg, masks):
+    case = C.masked_case(3, num_groups=4, m_max=192, n=256, k=384, masked_m=masks)
+    _check_masked(case, run_masked(fg, case))
+
+
+def test_masked_random_masks(fg):
+    case = C.masked_case(4, num_groups=6, m_max=256, n=384, k=256)
+    _check_masked(case, run_masked(fg, case))
+
+
+# -------------------------------------------------------------- K-grouped
+def run_k_grouped(fg, case, alias_c=False):
+    from gpu_util import GuardedOut, dev
+    g, m, n = case["g"], case["m"], case["n"]
+    d = GuardedOut(g * m, n, "f32")
+    c_t = None
+    if case["c"] is not None:
+        if alias_c:
+            d.fill_from(case["c"].reshape(g * m, n))
+            c_t = d.tensor.view(g, m, n)
+        else:
+            c_t = dev(case["c"])
+    fg.k_grouped_fp8_gemm_tn_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(case["ks"]), d.tensor.view(g, m, n), c=c_t)
+    _status_ok(fg)
+    d.check_guards()
+    return d
+
+
+@pytest.mark.parametrize("alias_c", [False, True])
+def test_k_grouped_parity(fg, alias_c):
+    case = C.k_grouped_case(5, num_groups=4, m=256, n=384, ks=[200, 0, 128, 300])
+    d = run_k_grouped(fg, case, alias_c)
+    ref = C.k_grouped_ref(case)
+    vals = d.values().reshape(case["g"], case["m"], case["n"])
+    for e in range(case["g"]):
+        C.compare(vals[e], ref[e], f"k-grouped group {e}")
+    # the empty segment copies C exactly
+    assert np.array_equal(vals[1], case["c"][1].astype(np.float64))
+
+
+def test_k_grouped_without_c_and_ragged_m(fg):
+    case = C.k_grouped_case(6, with_c=False, num_groups=3, m=208, n=144, ks=[128, 384, 5])
+    d = run_k_grouped(fg, case)
+    ref = C.k_grouped_ref(case)
+    vals = d.values().reshape(case["g"], case["m"], case["n"])
+    for e in range(case["g"]):
+        C.compare(vals[e], ref[e], f"k-grouped group {e}")
+
+
+def test_k_grouped_bad_segments_reported(fg):
+    from gpu_util import GuardedOut, dev
+    case = C.k_grouped_case(7, num_groups=2, m=128, n=128, ks=[128, 128])
+    d = GuardedOut(2 * 128, 128, "f32")
+    bad_ks = np.array([128, 64], np.int32)            # not a multiple of 128, wrong sum
+    fg.k_grouped_fp8_gemm_tn_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(bad_ks), d.tensor.view(2, 128, 128), c=dev(case["c"]))
+    st, detail = fg.get_device_error()
+    assert st == fg.FG_ERR_DEVICE_CONTRACT and detail == 0x104
+    assert np.all(d.is_sentinel())
