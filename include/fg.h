@@ -148,6 +148,36 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total,
                                         const int32_t* ks, const float* c, float* d,
                                         fg_stream_t stream);
 
+/*
+ * FP32 -> E4M3 quantisation with UE8M0 scales, written straight into the packed,
+ * MN-major, TMA-aligned scale layout the GEMMs above read.  The pages leave the FP8
+ * cast to the user and list layout helpers for it ("DeepGEMM Documentation", section
+ * 4 note on FP8 casting; section 10: transform_sf_into_required_layout,
+ * get_mn_major_tma_aligned_packed_ue8m0_tensor,
+ * get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor).
+ * Scale of a group: the smallest power of two 2^e with amax <= 448 * 2^e, stored as
+ * the byte e + 127 (clamped to [0, 254]; an all-zero group gets 127); code: E4M3
+ * round-to-nearest-even of x * 2^-e.  Bytes of missing tail groups in the last packed
+ * word are 0; the MN padding words of `sf` are not written.
+ * All arrays are device pointers, 16-byte aligned; asynchronous on `stream`.
+ */
+/* x [rows][K] FP32 -> q [rows][K] E4M3, sf [ceil(K/512)][align4(rows)] (1x128 groups
+ * along K per row: the activation scales of every NT GEMM).  K % 128 == 0. */
+int fg_quantize_1x128_rows(int rows, int K, const float* x, uint8_t* q, int32_t* sf,
+                           fg_stream_t stream);
+
+/* w [G][N][K] FP32 -> q [G][N][K] E4M3, sf [G][ceil(K/512)][align4(ceil(N/128))]
+ * (one scale per 128x128 block: the weight scales of the NT GEMMs).  K % 128 == 0; a
+ * ragged last row block takes its scale from its valid rows. */
+int fg_quantize_128x128_blocks(int G, int N, int K, const float* w, uint8_t* q, int32_t* sf,
+                               fg_stream_t stream);
+
+/* x [K][MN] FP32 -> q [K][MN] E4M3, sf [ceil(K/512)][align4(MN)] (1x128 groups along
+ * the leading K axis per column: both operands of the K-grouped GEMM; with zero-padded
+ * segments the packing is the K-grouped one).  K % 128 == 0, MN % 16 == 0. */
+int fg_quantize_1x128_cols(int K, int MN, const float* x, uint8_t* q, int32_t* sf,
+                           fg_stream_t stream);
+
 /* Row alignment of each group segment in the contiguous layout: 128, the M block
  * (docsearch section 9 item 2 and section 10). */
 int fg_get_mk_alignment_for_contiguous_layout(void);

@@ -30,6 +30,9 @@ _SIGNATURES = {
     "fg_m_grouped_fp8_gemm_nt_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
     "fg_k_grouped_fp8_gemm_tn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fg_quantize_1x128_rows": (_I, [_I, _I, _P, _P, _P, _P]),
+    "fg_quantize_128x128_blocks": (_I, [_I, _I, _I, _P, _P, _P, _P]),
+    "fg_quantize_1x128_cols": (_I, [_I, _I, _P, _P, _P, _P]),
     "fg_get_mk_alignment_for_contiguous_layout": (_I, []),
     "fg_get_tma_aligned_size": (_I, [_I, _I]),
     "fg_set_num_sms": (None, [_I]),
@@ -151,6 +154,36 @@ def k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, ks, d, c=None, stream=None)
     _check(lib.fg_k_grouped_fp8_gemm_tn_contiguous(g, m, n, k_total, _ptr(a), _ptr(sfa), _ptr(b),
                                                    _ptr(sfb), _ptr(ks), _ptr(c), _ptr(d),
                                                    _stream(stream)), "k_grouped_fp8_gemm_tn_contiguous")
+
+
+def _f32(t, name):
+    import torch
+    if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+        raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
+
+
+def quantize_1x128_rows(x, q, sf, stream=None) -> None:
+    """x [rows,K] FP32 -> q [rows,K] E4M3 bytes, sf [ceil(K/512), align4(rows)] packed UE8M0."""
+    _f32(x, "x"); _fp8(q, "q"); _i32(sf, "sf")
+    rows, k = x.shape
+    _check(lib.fg_quantize_1x128_rows(rows, k, _ptr(x), _ptr(q), _ptr(sf), _stream(stream)),
+           "quantize_1x128_rows")
+
+
+def quantize_128x128_blocks(w, q, sf, stream=None) -> None:
+    """w [G,N,K] (or [N,K]) FP32 -> q E4M3, sf [G, ceil(K/512), align4(ceil(N/128))]."""
+    _f32(w, "w"); _fp8(q, "q"); _i32(sf, "sf")
+    g, n, k = (1, *w.shape) if w.dim() == 2 else w.shape
+    _check(lib.fg_quantize_128x128_blocks(g, n, k, _ptr(w), _ptr(q), _ptr(sf), _stream(stream)),
+           "quantize_128x128_blocks")
+
+
+def quantize_1x128_cols(x, q, sf, stream=None) -> None:
+    """x [K,MN] FP32 -> q [K,MN] E4M3, sf [ceil(K/512), align4(MN)] (groups along K)."""
+    _f32(x, "x"); _fp8(q, "q"); _i32(sf, "sf")
+    k, mn = x.shape
+    _check(lib.fg_quantize_1x128_cols(k, mn, _ptr(x), _ptr(q), _ptr(sf), _stream(stream)),
+           "quantize_1x128_cols")
 
 
 def get_mk_alignment_for_contiguous_layout() -> int:
