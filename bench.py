@@ -1,0 +1,588 @@
+#!/usr/bin/env python
+"""Benchmark of the fine-grained FP8 GEMM library on one GB300 (or N replicas).
+
+Default workload (the headline metric's configuration): the dense FP8 NT GEMM pair
+  prefill  M=4096 N=7168 K=2048
+  decode   M=64   N=7168 K=4096
+with A scaled per 1x128 row group, B per 128x128 block (UE8M0), and an FP32 C
+accumulated into an FP32 D.  One step = one call of each.  Inputs are N(0,1) draws
+from a seeded torch generator on the GPU, quantised by the library's own quantise
+kernels; L2 is flushed (a write of twice its size) before every timed step, outside
+the timed events.
+
+Other workloads (--workload prefill | decode | contiguous | masked | k_grouped) time the
+single GEMMs on the same rules; they are measurement aids, the default line is the headline.
+
+Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
+CPU oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 GEMM TFLOPS (and HBM GB/s for small M) at 1 GB300 vs roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_tn.cu"]
+
+
+def align4(x: int) -> int:
+    return (x + 3) // 4 * 4
+
+
+def cdiv(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+# --------------------------------------------------------------------------- peaks
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:  # noqa: BLE001
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "moe_fp8_e4m3_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[workload][kernel]
+    except Exception:  # noqa: BLE001
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clock sampling
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for (t, r) in self.rows if t0 - 0.05 <= t <= t1 + 0.05]
+        note = "samples inside the timed region"
+        if not inside:
+            inside = [r for (_, r) in self.rows]
+            note = "timed region shorter than the sampling interval: samples around it"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = sorted(v for v in (num(r[2]) for r in inside) if v is not None)
+        mx = [num(r[3]) for r in inside if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for i, nm in enumerate(names):
+                if r[6 + i].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note,
+                "power_w_max": max((num(r[4]) or 0.0) for r in inside)}
+
+
+# ---------------------------------------------------------------------- workloads
+class DensePair:
+    """The headline workload: dense NT prefill + decode GEMMs, FP32 C -> FP32 D."""
+    name = "dense_pair"
+    description = ("dense FP8 NT GEMM pair: prefill M=4096 N=7168 K=2048 + decode M=64 N=7168 K=4096; "
+                   "A 1x128 / B 128x128 UE8M0 scales; FP32 C accumulated into FP32 D")
+    SHAPES = [("prefill", 4096, 7168, 2048), ("decode", 64, 7168, 4096)]
+
+    def __init__(self, torch, fg, seed):
+        import workloads
+        self.torch, self.fg = torch, fg
+        self.parts = []
+        for i, (nm, m, n, k) in enumerate(self.SHAPES):
+            xa = workloads.device_normal(seed + 10 * i, (m, k))
+            xb = workloads.device_normal(seed + 10 * i + 1, (n, k))
+            c = workloads.device_normal(seed + 10 * i + 2, (m, n))
+            a = torch.empty((m, k), dtype=torch.uint8, device="cuda")
+            sfa = torch.zeros((cdiv(k, 512), align4(m)), dtype=torch.int32, device="cuda")
+            b = torch.empty((n, k), dtype=torch.uint8, device="cuda")
+            sfb = torch.zeros((1, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
+            fg.quantize_1x128_rows(xa, a, sfa)
+            fg.quantize_128x128_blocks(xb, b, sfb)
+            del xa, xb
+            d = torch.empty((m, n), dtype=torch.float32, device="cuda")
+            flops = 2.0 * m * n * k
+            nbytes = m * k + n * k + sfa.numel() * 4 + sfb.numel() * 4 + 2 * m * n * 4
+            self.parts.append({"name": nm, "m": m, "n": n, "k": k, "a": a, "sfa": sfa, "b": b, "sfb": sfb[0],
+                               "c": c, "d": d, "flops": flops, "bytes": nbytes})
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda p=p: self.fg.fp8_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], c=p["c"])
+                for p in self.parts]
+
+    def e2e_io(self):
+        """(inputs as (device tensor, pinned host copy)), (outputs likewise)."""
+        ins, outs = [], []
+        for p in self.parts:
+            for key in ("a", "sfa", "b", "sfb", "c"):
+                ins.append((p[key], p[key].cpu().pin_memory()))
+            outs.append((p["d"], self.torch.empty_like(p["d"], device="cpu").pin_memory()))
+        return ins, outs
+
+    @classmethod
+    def oracle_inputs(cls):
+        """The same shapes for the CPU oracle: seeded numpy draws quantised by the oracle."""
+        from oracle import formats as F
+        import workloads
+        out = []
+        for i, (nm, m, n, k) in enumerate(cls.SHAPES):
+            w = workloads.dense(2000 + i, m, n, k, True)
+            a, sa = F.quantize_rows(w["a"])
+            b, sb = F.quantize_blocks(w["b"])
+            out.append({"m": m, "n": n, "k": k, "a": a, "sa": sa, "b": b, "sb": sb, "c": w["c"]})
+        return out
+
+    @classmethod
+    def oracle_full_step(cls):
+        """One full step of the oracle (both GEMMs, every output)."""
+        import oracle
+        from oracle import formats as F
+        items = []
+        for t in cls.oracle_inputs():
+            sfa, sfb = F.pack_ue8m0(t["sa"]), F.pack_ue8m0(t["sb"])
+            items.append((lambda t=t, sfa=sfa, sfb=sfb: oracle.fp8_gemm_nt(t["a"], sfa, t["b"], sfb, t["c"]),
+                          2.0 * t["m"] * t["n"] * t["k"]))
+        return items, "one full step (prefill 4096x7168x2048 + decode 64x7168x4096) per repetition"
+
+    @classmethod
+    def oracle_sub_step(cls, rows=32, cols=256):
+        """A bounded sample of one step: the first `rows` x `cols` outputs of each GEMM,
+        computed by the oracle on the corresponding slices of A, B, C and their scales."""
+        import oracle
+        from oracle import formats as F
+        items = []
+        for t in cls.oracle_inputs():
+            r, c = min(rows, t["m"]), min(cols, t["n"])
+            a, sfa = t["a"][:r], F.pack_ue8m0(t["sa"][:r])
+            b, sfb = t["b"][:c], F.pack_ue8m0(t["sb"][:cdiv(c, 128)])
+            cc = t["c"][:r, :c].copy()
+            items.append((lambda a=a, sfa=sfa, b=b, sfb=sfb, cc=cc: oracle.fp8_gemm_nt(a, sfa, b, sfb, cc),
+                          2.0 * r * c * t["k"]))
+        return items, f"per step: the first {rows} rows x {cols} columns of the prefill and decode outputs"
+
+
+class Contiguous:
+    name = "contiguous"
+    description = ("M-grouped contiguous FP8 NT GEMM: 32 experts of 256 (top-6 of 8192 tokens, experts 0-31 "
+                   "kept, 128-row padded segments, -1 padding rows), N=4096 K=4096, BF16 D")
+
+    def __init__(self, torch, fg, seed):
+        import numpy as np
+        import workloads
+        self.torch, self.fg = torch, fg
+        m_indices, row_token, counts = workloads.routing(workloads.rng(seed), 8192, 256, 6, 32)
+        m_total, n, k, g = len(m_indices), 4096, 4096, 32
+        x = workloads.device_normal(seed + 1, (8192, k))
+        xa = torch.zeros((m_total, k), dtype=torch.float32, device="cuda")
+        valid = np.nonzero(row_token >= 0)[0]
+        xa[torch.from_numpy(valid).cuda()] = x[torch.from_numpy(row_token[valid]).cuda()]
+        del x
+        self.a = torch.empty((m_total, k), dtype=torch.uint8, device="cuda")
+        self.sfa = torch.zeros((cdiv(k, 512), align4(m_total)), dtype=torch.int32, device="cuda")
+        fg.quantize_1x128_rows(xa, self.a, self.sfa)
+        del xa
+        pad = torch.from_numpy(np.nonzero(row_token < 0)[0]).cuda()
+        self.a[pad] = workloads.device_bytes(seed + 2, (len(pad), k))
+        self.b = torch.empty((g, n, k), dtype=torch.uint8, device="cuda")
+        self.sfb = torch.zeros((g, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
+        for e in range(g):
+            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
+            fg.quantize_128x128_blocks(xb, self.b[e:e + 1], self.sfb[e:e + 1])
+        self.m_indices = torch.from_numpy(m_indices).cuda()
+        self.d = torch.empty((m_total, n), dtype=torch.bfloat16, device="cuda")
+        nv = int(counts.sum())
+        used = int((counts > 0).sum())
+        self.flops = 2.0 * nv * n * k
+        self.bytes = (nv * k + used * n * k + self.sfa.numel() * 4 + self.sfb.numel() * 4 + nv * n * 2
+                      + m_total * 4)
+        self.parts = [{"name": "contiguous", "flops": self.flops, "bytes": self.bytes}]
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_gemm_nt_contiguous(self.a, self.sfa, self.b, self.sfb,
+                                                                 self.m_indices, self.d)]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.m_indices)]
+        return ins, [(self.d, self.torch.empty_like(self.d, device="cpu").pin_memory())]
+
+
+
+class Masked:
+    name = "masked"
+    description = ("M-grouped masked FP8 NT GEMM: 32 experts x 256 rows, masked_m ~ U{0..256} on the device, "
+                   "N=4096 K=2048, BF16 D")
+
+    def __init__(self, torch, fg, seed):
+        import numpy as np
+        import workloads
+        self.torch, self.fg = torch, fg
+        g, m_max, n, k = 32, 256, 4096, 2048
+        mm = workloads.rng(seed).integers(0, m_max + 1, g).astype(np.int32)
+        x = workloads.device_normal(seed + 1, (g * m_max, k))
+        self.a = torch.empty((g, m_max, k), dtype=torch.uint8, device="cuda")
+        self.sfa = torch.zeros((g, cdiv(k, 512), align4(m_max)), dtype=torch.int32, device="cuda")
+        for e in range(g):
+            fg.quantize_1x128_rows(x[e * m_max:(e + 1) * m_max], self.a[e], self.sfa[e])
+            if mm[e] < m_max:
+                self.a[e, mm[e]:] = workloads.device_bytes(seed + 50 + e, (m_max - mm[e], k))
+        del x
+        self.b = torch.empty((g, n, k), dtype=torch.uint8, device="cuda")
+        self.sfb = torch.zeros((g, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
+        for e in range(g):
+            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
+            fg.quantize_128x128_blocks(xb, self.b[e:e + 1], self.sfb[e:e + 1])
+        self.masked_m = torch.from_numpy(mm).cuda()
+        self.d = torch.empty((g, m_max, n), dtype=torch.bfloat16, device="cuda")
+        nv = int(mm.sum())
+        used = int((mm > 0).sum())
+        self.flops = 2.0 * nv * n * k
+        self.bytes = nv * k + used * n * k + nv * n * 2 + self.sfa.numel() * 4 + self.sfb.numel() * 4
+        self.parts = [{"name": "masked", "flops": self.flops, "bytes": self.bytes}]
+        self.expected_m = int(mm.mean())
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_gemm_nt_masked(self.a, self.sfa, self.b, self.sfb, self.masked_m,
+                                                             self.d, expected_m=self.expected_m)]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.masked_m)]
+        return ins, [(self.d, self.torch.empty_like(self.d, device="cpu").pin_memory())]
+
+
+class KGrouped:
+    name = "k_grouped"
+    description = ("K-grouped contiguous FP8 TN GEMM: 8 experts, M=4096 N=2048, K segments ~ Multinomial(16384) "
+                   "padded to 128, 1x128 scales along K, FP32 C accumulated into FP32 D")
+
+    def __init__(self, torch, fg, seed):
+        import numpy as np
+        import workloads
+        self.torch, self.fg = torch, fg
+        g, m, n = 8, 4096, 2048
+        ks_true = workloads.rng(seed).multinomial(16384, [1.0 / g] * g)
+        ks = (ks_true + 127) // 128 * 128
+        k_total = int(ks.sum())
+        xa = torch.zeros((k_total, m), dtype=torch.float32, device="cuda")
+        xb = torch.zeros((k_total, n), dtype=torch.float32, device="cuda")
+        off = 0
+        for e in range(g):
+            t = int(ks_true[e])
+            xa[off:off + t] = workloads.device_normal(seed + 10 + e, (t, m))
+            xb[off:off + t] = workloads.device_normal(seed + 30 + e, (t, n))
+            off += int(ks[e])
+        self.a = torch.empty((k_total, m), dtype=torch.uint8, device="cuda")
+        self.sfa = torch.zeros((cdiv(k_total, 512), align4(m)), dtype=torch.int32, device="cuda")
+        self.b = torch.empty((k_total, n), dtype=torch.uint8, device="cuda")
+        self.sfb = torch.zeros((cdiv(k_total, 512), align4(n)), dtype=torch.int32, device="cuda")
+        fg.quantize_1x128_cols(xa, self.a, self.sfa)
+        fg.quantize_1x128_cols(xb, self.b, self.sfb)
+        del xa, xb
+        self.ks = torch.from_numpy(ks.astype(np.int32)).cuda()
+        self.c = workloads.device_normal(seed + 60, (g, m, n))
+        self.d = torch.empty((g, m, n), dtype=torch.float32, device="cuda")
+        self.flops = 2.0 * m * n * float(ks_true.sum())
+        self.bytes = k_total * (m + n) + self.sfa.numel() * 4 + self.sfb.numel() * 4 + 2 * g * m * n * 4
+        self.parts = [{"name": "k_grouped", "flops": self.flops, "bytes": self.bytes}]
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.k_grouped_fp8_gemm_tn_contiguous(self.a, self.sfa, self.b, self.sfb, self.ks,
+                                                                 self.d, c=self.c)]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.ks, self.c)]
+        return ins, [(self.d, self.torch.empty_like(self.d, device="cpu").pin_memory())]
+
+
+class Prefill(DensePair):
+    """The prefill GEMM alone (profiling aid)."""
+    name = "prefill"
+    description = "dense FP8 NT GEMM M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
+    SHAPES = [("prefill", 4096, 7168, 2048)]
+
+
+class Decode(DensePair):
+    """The decode GEMM alone (profiling aid)."""
+    name = "decode"
+    description = "dense FP8 NT GEMM M=64 N=7168 K=4096, FP32 C accumulated into FP32 D"
+    SHAPES = [("decode", 64, 7168, 4096)]
+
+
+WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped)}
+
+
+# ------------------------------------------------------------------- CPU oracle arm
+def time_oracle(items, min_seconds=10.0, max_reps=8):
+    reps, flops, t0 = 0, 0.0, time.perf_counter()
+    while reps < max_reps:
+        for fn, f in items:
+            fn()
+            flops += f
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    return flops, time.perf_counter() - t0, reps
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    if args.workload != "dense_pair":
+        print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the dense_pair workload"}))
+        return 0
+    items, sample = DensePair.oracle_sub_step()
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        for fn, _f in items:
+            fn()
+    flops, t0 = 0.0, time.perf_counter()
+    for _ in range(args.steps):
+        for fn, f in items:
+            fn()
+            flops += f
+    t = time.perf_counter() - t0
+    value = flops / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded numpy N(0,1) draws quantised by the oracle",
+            "config": {"workload": DensePair.description},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import moe_fp8_e4m3_gb300 as fg
+
+    wl = WORKLOADS[args.workload](torch, fg, args.seed + 7919 * rank)
+    launches = wl.launches()
+    stream = torch.cuda.current_stream()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        for fn in launches:
+            fn()
+    st, detail = fg.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) during warm-up")
+
+    nl = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        for j, fn in enumerate(launches):
+            fn()
+            ev[i][j + 1].record(stream)
+    barrier()
+    t_wall1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    st, detail = fg.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({detail:#x}) in the timed region")
+
+    per_kernel = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
+                  for j in range(nl)]                      # ms, mean per launch
+    step_ms = sum(ev[i][0].elapsed_time(ev[i][nl]) for i in range(args.steps)) / args.steps
+    if dist is not None:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    flops_step = sum(p["flops"] for p in wl.parts)
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    ins, outs = wl.e2e_io()
+    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        k = i - 2
+        if k >= 0:
+            e0[k].record(stream)
+        for dt, ht in ins:
+            dt.copy_(ht, non_blocking=True)
+        for fn in launches:
+            fn()
+        for dt, ht in outs:
+            ht.copy_(dt, non_blocking=True)
+        if k >= 0:
+            e1[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    dom = max(range(nl), key=lambda j: per_kernel[j])
+    part = wl.parts[dom]
+    achieved = part["bytes"] / (per_kernel[dom] * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name, part["name"])
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    kernels = {}
+    for j, p in enumerate(wl.parts):
+        kernels[p["name"]] = {
+            "us_per_launch": round(per_kernel[j] * 1e3, 2),
+            "tflops": round(p["flops"] / (per_kernel[j] * 1e-3) / 1e12, 1),
+            "hbm_gbs": round(p["bytes"] / (per_kernel[j] * 1e-3) / 1e9, 1),
+            "algorithmic_bytes": p["bytes"], "flops": p["flops"],
+            "frac_of_hbm": round(p["bytes"] / (per_kernel[j] * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+            "frac_of_fp8_tensor": round(p["flops"] / (per_kernel[j] * 1e-3) / 1e12 / fp8_peak, 3),
+        }
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic: seeded N(0,1) draws (torch generator on the GPU) quantised by the library's "
+                "UE8M0 quantise kernels",
+        "config": {"workload": wl.description, "l2": "flushed before every timed step (write of 2x L2)",
+                   "replicas": world, "kernels": kernels},
+        "roofline": {"bound": "hbm", "kernel": part["name"], "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": part["bytes"],
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"},
+        "roofline_tensor": {"kernel": part["name"],
+                            "achieved": round(part["flops"] / (per_kernel[dom] * 1e-3) / 1e12, 1),
+                            "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                            "frac": round(part["flops"] / (per_kernel[dom] * 1e-3) / 1e12 / fp8_peak, 4),
+                            "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)"},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": nl * args.steps,
+        "cpu_baseline": None,
+    }
+    if world == 1 and not args.no_cpu_baseline and args.workload == "dense_pair":
+        items, sample = DensePair.oracle_full_step()
+        f, dt, reps = time_oracle(items)
+        line["cpu_baseline"] = {"value": round(f / dt / 1e12, 5), "unit": "TFLOP/s",
+                                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                                "sample": f"{sample}, {reps} repetition(s), {dt:.1f} s"}
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fg", "reference"], default="fg")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense_pair")
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

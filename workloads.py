@@ -47,15 +47,10 @@ def dense(seed: int, m: int, n: int, k: int, with_c: bool) -> dict:
     return out
 
 
-def contiguous(seed: int, num_tokens: int = 8192, num_routed: int = 256, topk: int = 6,
-               num_groups: int = 32, n: int = 4096, k: int = 4096, b_std: float = 0.02) -> dict:
-    """Routing structure and draws for the M-grouped contiguous layout.
-
-    Returns x (token activations), ``row_token`` (token index of each valid row, or -1),
-    ``m_indices`` (expert of each row, -1 for padding), per-expert ``counts``,
-    ``garbage`` bytes and scale bytes for padding rows, and the expert weights ``b``."""
-    g = rng(seed)
-    x = _normal(g, (num_tokens, k))
+def routing(g: np.random.Generator, num_tokens: int, num_routed: int, topk: int, num_groups: int):
+    """Uniform random logits, top-k experts per token; the rows routed to experts
+    0..num_groups-1 grouped by expert (ascending token order), each segment padded to a
+    multiple of 128 rows.  Returns (m_indices, row_token, counts)."""
     logits = g.random((num_tokens, num_routed), dtype=np.float32)
     top = np.argsort(-logits, axis=1, kind="stable")[:, :topk]
     m_indices, row_token, counts = [], [], []
@@ -65,12 +60,26 @@ def contiguous(seed: int, num_tokens: int = 8192, num_routed: int = 256, topk: i
         pad = (-len(toks)) % ALIGN
         m_indices += [e] * len(toks) + [-1] * pad
         row_token += list(toks) + [-1] * pad
+    return (np.array(m_indices, dtype=np.int32), np.array(row_token, dtype=np.int64),
+            np.array(counts, dtype=np.int64))
+
+
+def contiguous(seed: int, num_tokens: int = 8192, num_routed: int = 256, topk: int = 6,
+               num_groups: int = 32, n: int = 4096, k: int = 4096, b_std: float = 0.02) -> dict:
+    """Routing structure and draws for the M-grouped contiguous layout.
+
+    Returns x (token activations), ``row_token`` (token index of each valid row, or -1),
+    ``m_indices`` (expert of each row, -1 for padding), per-expert ``counts``,
+    ``garbage`` bytes and scale bytes for padding rows, and the expert weights ``b``."""
+    g = rng(seed)
+    x = _normal(g, (num_tokens, k))
+    m_indices, row_token, counts = routing(g, num_tokens, num_routed, topk, num_groups)
     m_total = len(m_indices)
     return {
         "x": x,
-        "m_indices": np.array(m_indices, dtype=np.int32),
-        "row_token": np.array(row_token, dtype=np.int64),
-        "counts": np.array(counts, dtype=np.int64),
+        "m_indices": m_indices,
+        "row_token": row_token,
+        "counts": counts,
         "garbage": g.integers(0, 256, (m_total, k), dtype=np.uint8),
         "garbage_sf": g.integers(0, 256, (m_total, k // ALIGN), dtype=np.uint8),
         "b": _normal(g, (num_groups, n, k), b_std),
@@ -115,3 +124,24 @@ def k_grouped(seed: int, num_groups: int = 8, m: int = 4096, n: int = 2048,
         off += int(ks_pad[e])
     return {"a": a, "b": b, "ks": ks_pad.astype(np.int32), "ks_true": ks_true,
             "c": _normal(g, (num_groups, m, n))}
+
+
+def device_normal(seed: int, shape, std: float = 1.0, device: str = "cuda"):
+    """N(0, std^2) float32 draws made on the GPU by torch's seeded generator, for
+    benchmark inputs too large to draw on the host.  (Seeded and reproducible on one
+    machine; not the same numbers as the numpy draws above.)"""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x
+
+
+def device_bytes(seed: int, shape, device: str = "cuda"):
+    """Uniform random bytes on the GPU (garbage rows)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return torch.randint(0, 256, tuple(shape), generator=gen, device=device, dtype=torch.uint8)
