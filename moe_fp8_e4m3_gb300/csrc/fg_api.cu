@@ -100,6 +100,28 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
     return r == CUDA_SUCCESS;
 }
 
+// 3-D tiled tensor map over [outer2][outer1][inner] (pitches in bytes).
+bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t outer1, uint64_t outer2, uint64_t pitch1, uint64_t pitch2, uint32_t box_inner,
+               uint32_t box_outer1, CUtensorMapSwizzle swizzle) {
+    cuuint64_t dims[3] = {inner, outer1, outer2};
+    cuuint64_t strides[2] = {pitch1, pitch2};
+    cuuint32_t box[3] = {box_inner, box_outer1, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box,
+                                elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// C/D maps of a [rows][N] output: boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16
+// columns), 128-byte swizzle, matching the epilogue's shared-memory slots.
+bool encode_out_2d(CUtensorMap* map, const void* base, int n, long long rows, bool f32) {
+    const uint32_t esz = f32 ? 4 : 2;
+    return encode_2d(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base,
+                     (uint64_t)n, (uint64_t)rows, (uint64_t)n * esz, 128 / esz, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool print_configs() {
     const char* e = std::getenv("FG_PRINT_CONFIGS");
     return e && e[0] == '1';
@@ -111,20 +133,29 @@ int forced_bn() {
     return e ? std::atoi(e) : 0;
 }
 
-// N-tile choice: the widest tile that still gives every SM at least one tile; narrower
-// tiles when the problem has too few row blocks to fill the GPU.
-int choose_bn_nt(long long row_blocks, int n, int sms) {
+// N-tile choice.  Cost model: the busiest SM runs ceil(tiles / SMs) tiles, each costing
+// about (BN + 32) column units (the 32 stands for the A re-read and fixed per-tile work).
+// With a C/D-heavy epilogue only double-buffered tile widths (BN <= 224) are considered,
+// so the epilogue of one tile overlaps the MMAs of the next.
+int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     const int f = forced_bn();
-    if (f == 64 || f == 128 || f == 256) return f;
-    for (int bn : {256, 128}) {
-        if (row_blocks * ceil_div(n, bn) >= sms) return bn;
+    if (f == 64 || f == 128 || f == 192 || f == 224 || f == 256) return f;
+    int best = 128;
+    long long best_cost = -1;
+    for (int bn : {256, 224, 192, 128, 64}) {
+        if (heavy_epilogue && bn == 256) continue;
+        const long long tiles = row_blocks * ceil_div(n, bn);
+        const long long waves = (tiles + sms - 1) / sms;
+        const long long cost = waves * (bn + 32);
+        if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
     }
-    return 64;
+    return best;
 }
 
-int choose_bn_tn(long long row_blocks, int n, int sms) {
+int choose_bn_tn(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     const int f = forced_bn();
     if (f == 128 || f == 256) return f;
+    if (heavy_epilogue) return 128;
     return row_blocks * ceil_div(n, 256) >= sms ? 256 : 128;
 }
 
@@ -134,13 +165,15 @@ void fill_common(GemmParams& p, const DeviceState& st) {
     p.debug_stall = g_debug_stall;
 }
 
-int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
-              cudaStream_t s) {
+int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+              const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
     cudaError_t e;
     switch (bn) {
-        case 64: e = fg::launch_gemm<64, false>(p, ma, mb, grid, s); break;
-        case 128: e = fg::launch_gemm<128, false>(p, ma, mb, grid, s); break;
-        default: e = fg::launch_gemm<256, false>(p, ma, mb, grid, s); break;
+        case 64: e = fg::launch_gemm<64, false>(p, ma, mb, mc, md, grid, s); break;
+        case 128: e = fg::launch_gemm<128, false>(p, ma, mb, mc, md, grid, s); break;
+        case 192: e = fg::launch_gemm<192, false>(p, ma, mb, mc, md, grid, s); break;
+        case 224: e = fg::launch_gemm<224, false>(p, ma, mb, mc, md, grid, s); break;
+        default: e = fg::launch_gemm<256, false>(p, ma, mb, mc, md, grid, s); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -149,10 +182,10 @@ int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensor
     return FG_OK;
 }
 
-int launch_tn(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
-              cudaStream_t s) {
-    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, ma, mb, grid, s)
-                                    : fg::launch_gemm<256, true>(p, ma, mb, grid, s);
+int launch_tn(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+              const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
+    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, ma, mb, mc, md, grid, s)
+                                    : fg::launch_gemm<256, true>(p, ma, mb, mc, md, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -187,7 +220,7 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
-    const int bn = choose_bn_nt(num_mb, N, sms);
+    const int bn = choose_bn_nt(num_mb, N, sms, c != nullptr);
     GemmParams p{};
     p.kind = fg::kDense;
     p.M = M; p.N = N; p.K = K; p.G = 1;
@@ -196,17 +229,19 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
     p.sfa_rows = M;
-    p.c = c; p.d = d;
+    p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc, md;
+    std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d tiles=%lld grid=%d\n", M, N, K, bn, tiles, grid);
-    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
@@ -223,7 +258,7 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = M_total / 128;
-    const int bn = choose_bn_nt(num_mb, N, sms);
+    const int bn = choose_bn_nt(num_mb, N, sms, false);
     GemmParams p{};
     p.kind = fg::kContiguous;
     p.M = M_total; p.N = N; p.K = K; p.G = G;
@@ -236,16 +271,18 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     p.m_indices = m_indices;
     p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc, md;
+    std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_out_2d(&md, d, N, M_total, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
                      M_total, N, K, G, bn, grid);
-    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
@@ -261,7 +298,7 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int hint = expected_m > 0 ? (expected_m < M_max ? expected_m : M_max) : M_max;
-    const int bn = choose_bn_nt((long long)G * ceil_div(hint, 128), N, sms);
+    const int bn = choose_bn_nt((long long)G * ceil_div(hint, 128), N, sms, false);
     GemmParams p{};
     p.kind = fg::kMasked;
     p.M = M_max; p.N = N; p.K = K; p.G = G;
@@ -275,15 +312,17 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     p.masked_m = masked_m;
     p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc, md;
+    std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_out_2d(&md, d, N, (long long)G * M_max, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)G * p.num_mb * p.num_nb;   // upper bound
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_masked G=%d M_max=%d N=%d K=%d BN=%d grid=%d\n", G, M_max, N, K, bn, grid);
-    return launch_nt(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const uint8_t* a,
@@ -303,7 +342,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
-    const int bn = choose_bn_tn((long long)G * num_mb, N, sms);
+    const int bn = choose_bn_tn((long long)G * num_mb, N, sms, true);
     GemmParams p{};
     p.kind = fg::kKGrouped;
     p.M = M; p.N = N; p.K = K_total; p.G = G;
@@ -313,11 +352,18 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     p.sfa_ld = align4(M); p.sfb_ld = align4(N);
     p.sfa_rows = M;
     p.ks = ks;
-    p.c = c; p.d = d;
+    p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc, md;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
+    std::memset(&mc, 0, sizeof(mc));
+    // C and D as [G][M][N]: boxes never cross into the next group's rows.
+    const uint64_t pitch1 = (uint64_t)N * 4, pitch2 = (uint64_t)M * N * 4;
+    if (!encode_3d(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, d, N, M, G, pitch1, pitch2, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (c && !encode_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M, G, pitch1, pitch2, 32, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B)))
+        return FG_ERR_INVALID_ARG;
     // With K_total == 0 every segment is empty and no operand load is ever issued.
     if (K_total > 0 &&
         (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K_total, M, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -327,7 +373,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] k_grouped_tn G=%d M=%d N=%d K_total=%d BN=%d grid=%d\n", G, M, N, K_total, bn, grid);
-    return launch_tn(bn, p, ma, mb, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_tn(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_get_mk_alignment_for_contiguous_layout(void) { return 128; }

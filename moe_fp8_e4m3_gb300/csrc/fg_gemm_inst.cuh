@@ -10,7 +10,7 @@ namespace fg {
 
 template <int BN, bool kTN>
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        int grid, cudaStream_t stream) {
+                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream) {
     constexpr int kSmem = TileCfg<BN>::kSmemBytes;
     auto kernel = fg_gemm_kernel<BN, kTN>;
     int dev = 0;
@@ -32,7 +32,7 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUt
     cfg.blockDim = dim3(224);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, kernel, p, map_a, map_b);
+    return cudaLaunchKernelEx(&cfg, kernel, p, map_a, map_b, map_c, map_d);
 }
 
 }  // namespace fg

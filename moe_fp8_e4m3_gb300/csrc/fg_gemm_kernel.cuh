@@ -12,19 +12,26 @@
 // loop, so every partial sum is promoted to FP32 with its scale already applied (the
 // pages' "two-level accumulation", Deepseek AI Libera DeepGEMM article, section
 // "Details and technical benefits", realised by the hardware's scaled MMA instead of a
-// CUDA-core FMA pass).
+// CUDA-core FMA pass).  A packed UE8M0 word holds the scales of four consecutive
+// K-groups; it is copied to TMEM unchanged and the MMA's scale-factor byte selector
+// picks byte (g mod 4).
 //
 // Warp roles (224 threads):
 //   warp 0      TMA producer: A and B tiles into a ring of shared-memory stages
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
-//   warp 2      scale loader: packed UE8M0 words into the tcgen05.cp layout
-//   warps 3..6  epilogue: TMEM -> registers (+C) -> BF16/FP32 -> global memory
+//   warp 2      scale loader: packed UE8M0 words into the tcgen05.cp layout, one packed
+//               word ahead (the loads of the next word are in flight while the current
+//               one is written into up to four stages)
+//   warps 3..6  epilogue: TMEM -> registers, + C (TMA-prefetched into shared memory),
+//               -> BF16/FP32 -> swizzled shared-memory slot -> TMA store
+// Accumulators are double-buffered in TMEM when two fit next to the scale slots
+// (BN <= 224), so the epilogue of one tile overlaps the MMAs of the next.
 // Every role walks the same static persistent tile sequence (tile = blockIdx.x +
 // i * gridDim.x), decoded from device-resident segment data without host sync.
 //
 // Every wait is bounded (globaltimer); on expiry the CTA records a time-out in the
 // device status word, raises a shared abort flag that every other wait observes,
-// drains its own in-flight tensor-core work and TMA loads (again bounded), frees TMEM
+// drains its own in-flight tensor-core work and TMA copies (again bounded), frees TMEM
 // and returns.  Nothing traps.
 #pragma once
 
@@ -46,9 +53,11 @@ enum : int {
     kChkMaskRange = 3,         // masked_m outside [0, M_max]
     kChkKSegments = 4,         // ks not multiples of 128 / negative / wrong sum
     kWaitProducer = 1, kWaitMma = 2, kWaitScales = 3, kWaitEpilogue = 4, kWaitDrain = 5,
+    kWaitEpilogueC = 6,
 };
 
-constexpr int kMaxGroups = 1024;  // masked / K-grouped groups held in shared memory
+constexpr int kMaxGroups = 512;   // masked / K-grouped groups held in shared memory
+constexpr int kSmemLimit = 232448;
 
 struct GemmParams {
     int kind;
@@ -64,8 +73,7 @@ struct GemmParams {
     const int32_t* m_indices;
     const int32_t* masked_m;
     const int32_t* ks;
-    const float* c;
-    void* d;
+    void* d;               // for the per-thread store path (partially valid row groups)
     int* status;
     unsigned long long timeout_ns;
     int debug_stall;
@@ -75,28 +83,37 @@ template <int BN>
 struct TileCfg {
     static constexpr int kBM = 128, kBK = 128;
     static constexpr int kSfbAtoms = (BN + 127) / 128;
-    static constexpr int kSfCols = 4 + 4 * kSfbAtoms;   // TMEM columns of one scale slot
-    static constexpr int kNumAcc = (2 * BN + 2 * kSfCols <= 512) ? 2 : 1;
-    static constexpr int kSfCol0 = kNumAcc * BN;
-    static constexpr int kABytes = kBM * kBK;             // 16 KB
+    static constexpr int kSfCols = 4 + 4 * kSfbAtoms;    // TMEM columns of one scale slot
+    static constexpr int kNumAcc = (2 * BN + 32 <= 512) ? 2 : 1;
+    static constexpr int kSfCol0 = (kNumAcc * BN + 15) / 16 * 16;
+    static_assert(kSfCol0 + 16 + kSfCols <= 512, "TMEM columns");
+    static constexpr int kABytes = kBM * kBK;              // 16 KB
     static constexpr int kBBytes = BN * kBK;
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = kSfbAtoms * 512;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-    static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+    // Epilogue: per warp, kSlots shared-memory slots of 32 rows x 128 bytes.
+    static constexpr int kSlots = BN >= 256 ? 1 : 4;
+    static constexpr int kSlotBytes = 4096;
+    static constexpr int kEpiBytes = 4 * kSlots * kSlotBytes;
+    static constexpr int kMiscBytes = 1024 + 2 * (kMaxGroups + 1) * 4;   // barriers etc. + group tables
+    static constexpr int kStages0 = (kSmemLimit - 1024 - kEpiBytes - kMiscBytes) / kStageBytes;
     static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
-    static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+    static constexpr int kOffEpi = kOffB + kStages * kBBytes;                 // 1024-aligned
+    static constexpr int kOffSfa = kOffEpi + kEpiBytes;
     static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
     static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;        // tmem addr, abort flag
-    static constexpr int kOffSched = kOffMisc + 16;                // int[kMaxGroups + 1]
+    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1 + 4 * kSlots;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;                   // tmem addr, abort flag
+    static constexpr int kOffSched = kOffMisc + 16;                           // int[kMaxGroups + 1]
     static constexpr int kOffCnt = kOffSched + (kMaxGroups + 1) * 4;
-    static constexpr int kSmemBytes = kOffCnt + kMaxGroups * 4 + 1024;  // + alignment slack
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-    static_assert(kSmemBytes <= 232448, "shared memory");
+    static constexpr int kSmemBytes = kOffCnt + kMaxGroups * 4 + 1024;       // + alignment slack
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128 (and 32-column chunks)");
+    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kNumBars * 8 <= 1024 - 16, "barrier area");
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
 };
 
 struct Tile {
@@ -104,7 +121,8 @@ struct Tile {
     int a_coord, b_coord;   // NT: rows in the A/B maps; TN: columns (m0 / n0)
     int kb0, nkb;           // first global K-group and number of K-groups
     int valid_rows;         // rows [0, valid_rows) of the tile lie inside the problem
-    long long d_row;        // row of D (and C) that holds the tile's row 0
+    long long d_row;        // row of D (flat [rows][N] view) that holds the tile's row 0
+    int d_y, d_z;           // coordinates of row 0 in the C/D tensor maps
     int sfa_g, sfa_row;
     bool skip;
 };
@@ -135,6 +153,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
     }
 }
 
+// Wait without abort observation, for draining in-flight copies on the way out.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < limit_ns) {
+    }
+}
+
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const int* sched,
                                             const int* cnt, int& cursor) {
@@ -144,6 +169,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
     tl.kb0 = 0;
     tl.nkb = p.K / 128;
     tl.sfa_g = 0;
+    tl.d_z = 0;
     if (p.kind == kDense) {
         const int mb = t % p.num_mb, nb = t / p.num_mb;
         tl.n0 = nb * BN;
@@ -160,7 +186,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
             if (g >= p.G) record_status(p.status, kErrContract | kChkGroupIndex);
             tl.skip = true;
         }
-        tl.g = g < 0 ? 0 : (g >= p.G ? 0 : g);
+        tl.g = (g < 0 || g >= p.G) ? 0 : g;
         tl.a_coord = mb * 128;
         tl.b_coord = tl.g * p.N + tl.n0;
         tl.valid_rows = 128;
@@ -191,15 +217,62 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
         tl.nkb = sched[g + 1] - sched[g];
         tl.valid_rows = min(128, p.M - mb * 128);
         tl.d_row = (long long)g * p.M + mb * 128;
+        tl.d_y = mb * 128;
+        tl.d_z = g;
         tl.sfa_row = mb * 128;
+        return tl;
     }
+    tl.d_y = static_cast<int>(tl.d_row);
     return tl;
 }
+
+// Walks the tiles of one CTA, skipping the ones no role works on.
+template <int BN>
+struct TileIter {
+    int t;
+    int cursor;
+    __device__ __forceinline__ bool next(const GemmParams& p, int total, const int* sched, const int* cnt,
+                                         Tile& tl) {
+        while (t < total) {
+            tl = decode_tile<BN>(p, t, sched, cnt, cursor);
+            t += gridDim.x;
+            if (!tl.skip) return true;
+        }
+        return false;
+    }
+};
+
+// Scale words of one packed word `kw` of one tile: 4 SFA words and 4 per 128-row SFB
+// atom for this lane (MN index j * 32 + lane of each atom).
+template <int BN, bool kTN>
+struct ScaleWords {
+    static constexpr int kAtoms = (BN + 127) / 128;
+    int a[4];
+    int b[kAtoms][4];
+    __device__ __forceinline__ void load(const GemmParams& p, const Tile& tl, int kw, int lane) {
+        const int32_t* pa = p.sfa + tl.sfa_g * p.sfa_gstride + (long long)kw * p.sfa_ld;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int row = tl.sfa_row + lane + 32 * j;
+            a[j] = row < p.sfa_rows ? __ldg(pa + row) : 0;
+        }
+        const int32_t* pb = p.sfb + tl.g * p.sfb_gstride + (long long)kw * p.sfb_ld;
+#pragma unroll
+        for (int i = 0; i < kAtoms; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = tl.n0 + i * 128 + j * 32 + lane;
+                b[i][j] = n < p.N ? __ldg(pb + (kTN ? n : (n >> 7))) : 0;
+            }
+        }
+    }
+};
 
 template <int BN, bool kTN>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
-               const __grid_constant__ CUtensorMap tm_b) {
+               const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+               const __grid_constant__ CUtensorMap tm_d) {
     using C = TileCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -211,7 +284,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kNumAcc + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc);
+    const uint32_t mma_drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc);
+    auto cfull_bar = [&](int ew, int slot) {
+        return bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + ew * C::kSlots + slot);
+    };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     int* sched = reinterpret_cast<int*>(smem + C::kOffSched);
@@ -227,13 +303,16 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 4);     // one arrive per epilogue warp
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(mma_drain_bar, 1);
+        for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
         *abort_flag = 0;
         fence_mbar_init();
         if (p.K > 0) {          // a K-grouped call with K_total == 0 has no operand maps
             tma_prefetch_map(&tm_a);
             tma_prefetch_map(&tm_b);
         }
+        tma_prefetch_map(&tm_d);
+        if (p.has_c) tma_prefetch_map(&tm_c);
     }
     // Group tables for the masked (tile prefix) and K-grouped (K-group prefix) layouts.
     int total_tiles = p.num_mb * p.num_nb;
@@ -284,13 +363,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    bool invalid = false;
     if (p.kind == kMasked) total_tiles = sched[p.G];
-    if (p.kind == kKGrouped) {
-        invalid = sched[p.G] < 0;
-        total_tiles = p.G * p.num_mb * p.num_nb;
-    }
-    if (invalid) total_tiles = 0;
+    if (p.kind == kKGrouped) total_tiles = sched[p.G] < 0 ? 0 : p.G * p.num_mb * p.num_nb;
 
     const WaitCtl wctl{abort_flag, p.status, p.timeout_ns};
 
@@ -299,13 +373,12 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            int cursor = 0;
             bool stall = p.debug_stall != 0;
             uint32_t armed = 0, armed_par = 0;   // per-stage: armed at least once / parity
             bool aborted = false;
-            for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-                const Tile tl = decode_tile<BN>(p, t, sched, cnt, cursor);
-                if (tl.skip) continue;
+            TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+            Tile tl;
+            while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
                 for (int kb = 0; kb < tl.nkb; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
                     if (stall) {
@@ -333,14 +406,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             }
             if (aborted || *abort_flag) {
                 // Bounded drain of loads that may still be landing in shared memory.
-                WaitCtl quick{abort_flag, p.status, 20000000ull};
-                int dummy = 0;
-                for (int i = 0; i < C::kStages; ++i) {
-                    if (!(armed >> i & 1u)) continue;
-                    const uint32_t par = armed_par >> i & 1u;
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(full_bar(i), par) && globaltimer_ns() - t0 < quick.timeout_ns) ++dummy;
-                }
+                for (int i = 0; i < C::kStages; ++i)
+                    if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
             }
         }
     } else if (warp == 1) {
@@ -351,12 +418,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
-            int cursor = 0;
             uint32_t kcount = 0;
             bool aborted = false;
-            for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-                const Tile tl = decode_tile<BN>(p, t, sched, cnt, cursor);
-                if (tl.skip) continue;
+            TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+            Tile tl;
+            while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
                 if (!wait_bar(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_t = tmem_base + acc * BN;
@@ -364,7 +430,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     if (!wait_bar(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
                     tc_fence_after();
                     const uint32_t slot = kcount & 1u;
-                    const uint32_t sfa_t = tmem_base + C::kSfCol0 + slot * C::kSfCols;
+                    const uint32_t sfa_t = tmem_base + C::kSfCol0 + slot * 16;
                     const uint32_t sfb_t = sfa_t + 4;
                     const uint32_t ssfa = sbase + C::kOffSfa + s * C::kSfaBytes;
                     const uint32_t ssfb = sbase + C::kOffSfb + s * C::kSfbBytes;
@@ -397,71 +463,113 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
             // Wait (bounded) until every tensor-core operation issued here has finished.
-            tc_commit(drain_bar);
+            tc_commit(mma_drain_bar);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(drain_bar, 0)) {
+            while (!mbar_try_wait(mma_drain_bar, 0)) {
                 if (globaltimer_ns() - t0 > p.timeout_ns) { record_status(p.status, kErrTimeout | kWaitDrain); break; }
             }
         }
         __syncwarp();
     } else if (warp == 2) {
         // ----------------------------------------------------- scale loader
+        // Units: (tile, packed word kw) covering up to four consecutive K-groups.  The
+        // words of the next unit are loaded while the current one fills its stages.
         int s = 0;
         uint32_t ph = 0;
-        int cursor = 0;
-        bool aborted = false;
-        for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-            const Tile tl = decode_tile<BN>(p, t, sched, cnt, cursor);
-            if (tl.skip) continue;
-            for (int kb = 0; kb < tl.nkb; ++kb) {
+        TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+        Tile tl, tn;
+        bool have = false;
+        while ((have = it.next(p, total_tiles, sched, cnt, tl)) && tl.nkb == 0) {
+        }
+        int kb = 0;
+        ScaleWords<BN, kTN> cur, nxt;
+        if (have) cur.load(p, tl, tl.kb0 >> 2, lane);
+        while (have) {
+            // the unit after the current one: same tile, next word; or the next tile's first
+            const int kw = (tl.kb0 + kb) >> 2;
+            const int kb_end = min(tl.nkb, (kw + 1) * 4 - tl.kb0);
+            bool have_next;
+            int next_kb;
+            if (kb_end < tl.nkb) {
+                tn = tl;
+                next_kb = kb_end;
+                have_next = true;
+            } else {
+                while ((have_next = it.next(p, total_tiles, sched, cnt, tn)) && tn.nkb == 0) {
+                }
+                next_kb = 0;
+            }
+            if (have_next) nxt.load(p, tn, (tn.kb0 + next_kb) >> 2, lane);
+            bool aborted = false;
+            for (; kb < kb_end; ++kb) {
                 // warp-uniform decision: every lane leaves together on abort
                 const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                const int kw = (tl.kb0 + kb) >> 2;
-                const int32_t* pa = p.sfa + tl.sfa_g * p.sfa_gstride + (long long)kw * p.sfa_ld;
-                int4 va;
-                {
-                    int v[4];
+                // word (lane, j) of each 32x4 atom holds MN index j * 32 + lane
+                *reinterpret_cast<int4*>(smem + C::kOffSfa + s * C::kSfaBytes + lane * 16) =
+                    make_int4(cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int row = tl.sfa_row + lane + 32 * j;
-                        v[j] = row < p.sfa_rows ? __ldg(pa + row) : 0;
-                    }
-                    va = make_int4(v[0], v[1], v[2], v[3]);
-                }
-                // word (lane, j) of the 32x4 atom holds MN index j * 32 + lane
-                *reinterpret_cast<int4*>(smem + C::kOffSfa + s * C::kSfaBytes + lane * 16) = va;
-                const int32_t* pb = p.sfb + tl.g * p.sfb_gstride + (long long)kw * p.sfb_ld;
-#pragma unroll
-                for (int i = 0; i < C::kSfbAtoms; ++i) {
-                    int v[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int n = tl.n0 + i * 128 + j * 32 + lane;
-                        v[j] = n < p.N ? __ldg(pb + (kTN ? n : (n >> 7))) : 0;
-                    }
+                for (int i = 0; i < C::kSfbAtoms; ++i)
                     *reinterpret_cast<int4*>(smem + C::kOffSfb + s * C::kSfbBytes + i * 512 + lane * 16) =
-                        make_int4(v[0], v[1], v[2], v[3]);
-                }
+                        make_int4(cur.b[i][0], cur.b[i][1], cur.b[i][2], cur.b[i][3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_bar(s));
                 if (++s == C::kStages) { s = 0; ph ^= 1u; }
             }
+            if (aborted) break;
+            have = have_next;
+            tl = tn;
+            kb = next_kb;
+            cur = nxt;
         }
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM sub-partition this warp may read
+        const int ew = warp - 3;                // epilogue warp index (slot region)
         const int row = q * 32 + lane;
+        const bool f32 = p.d_f32 != 0;
+        const int cw = f32 ? 32 : 64;           // columns per chunk: 128 bytes per row
+        const uint32_t slot0 = sbase + C::kOffEpi + ew * C::kSlots * C::kSlotBytes;
+        uint8_t* slot0_ptr = smem + C::kOffEpi + ew * C::kSlots * C::kSlotBytes;
+        const bool kg = p.kind == kKGrouped;
+
+        // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
+        TileIter<BN> cit{static_cast<int>(blockIdx.x), 0};
+        Tile ctl;
+        bool c_have = p.has_c ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
+        int c_chunk = 0;
+        uint32_t c_issued = 0;       // chunks whose C load has been issued
+        auto issue_c = [&](uint32_t chunk_id) {
+            // chunk_id-th chunk of this warp's stream goes to slot chunk_id % kSlots
+            const int nch = (min(BN, p.N - ctl.n0) + 31) / 32;
+            const int sl = static_cast<int>(chunk_id % C::kSlots);
+            const uint32_t dst = slot0 + sl * C::kSlotBytes;
+            const uint32_t bar = cfull_bar(ew, sl);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, C::kSlotBytes);
+            const int x = ctl.n0 + c_chunk * 32;
+            if (kg) tma_load_3d(dst, &tm_c, bar, x, ctl.d_y + q * 32, ctl.d_z);
+            else tma_load_2d(dst, &tm_c, bar, x, ctl.d_y + q * 32);
+            if (++c_chunk == nch) {
+                c_chunk = 0;
+                c_have = cit.next(p, total_tiles, sched, cnt, ctl);
+            }
+        };
+        if (lane == 0) {
+            while (c_have && c_issued + 1 < static_cast<uint32_t>(C::kSlots)) issue_c(c_issued++);
+        }
+
         int acc = 0;
         uint32_t acc_ph = 0;
-        int cursor = 0;
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const Tile tl = decode_tile<BN>(p, t, sched, cnt, cursor);
-            if (tl.skip) continue;
+        uint32_t chunk_id = 0;       // chunks consumed so far
+        bool aborted = false;
+        TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+        Tile tl;
+        while (it.next(p, total_tiles, sched, cnt, tl)) {
             // warp-uniform decision before the .sync.aligned TMEM loads below
             const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
             tc_fence_after();
             const long long grow = tl.d_row + row;
             bool row_ok = row < tl.valid_rows;
@@ -470,75 +578,140 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                 if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
                 row_ok = (mi == tl.g);
             }
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                const int n = tl.n0 + c0;
-                if (n >= p.N) break;
-                uint32_t r[32];
+            // Rows past the end of the D tensor are clipped by the TMA store; the masked and
+            // contiguous layouts have rows inside D that must stay untouched.
+            const bool use_tma = (p.kind == kDense || kg) || __all_sync(0xffffffffu, row_ok);
+            const int ncols = min(BN, p.N - tl.n0);
+            const int nch = (ncols + cw - 1) / cw;
+            for (int ch = 0; ch < nch; ++ch, ++chunk_id) {
+                const int c0 = ch * cw;
+                const int sl = static_cast<int>(chunk_id % C::kSlots);
+                const uint32_t sl_addr = slot0 + sl * C::kSlotBytes;
+                uint8_t* sl_ptr = slot0_ptr + sl * C::kSlotBytes;
+                uint32_t r[64];
                 if (tl.nkb > 0) {
-                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0, r);
+                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0,
+                                       *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    if (!f32 && c0 + 32 < BN)
+                        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0 + 32,
+                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    for (int i = 0; i < 64; ++i) r[i] = 0u;
                 }
-                if (!row_ok) continue;
-                float v[32];
+                if (!f32 && !(c0 + 32 < BN)) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                const int halves = (p.N - n) >= 32 ? 2 : 1;
-                if (p.has_c) {
-                    const float* cp = p.c + grow * p.N + n;
+                    for (int i = 32; i < 64; ++i) r[i] = 0u;
+                }
+                if (ch == nch - 1) {
+                    // the accumulator buffer is free once its last columns are in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                }
+                // A 64-column BF16 chunk at the end of a BN = 224 tile would store into the
+                // neighbouring tile: such a chunk takes the per-thread path (no C in BF16).
+                if (use_tma && c0 + cw <= BN) {
+                    if (p.has_c) {
+                        if (lane == 0 && c_issued == chunk_id && c_have) {
+                            // not prefetched (single slot): load now, once the slot's last store is read
+                            bulk_wait_group_read<0>();
+                            issue_c(c_issued++);
+                        }
+                        __syncwarp();
+                        const bool okc = wait_bar(cfull_bar(ew, sl), (chunk_id / C::kSlots) & 1u, wctl, kWaitEpilogueC);
+                        if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
+                    } else {
+                        // the slot's previous store (kSlots chunks ago) must have been read
+                        if (lane == 0) {
+                            if (C::kSlots == 1) bulk_wait_group_read<0>();
+                            else bulk_wait_group_read<C::kSlots - 1>();
+                        }
+                        __syncwarp();
+                    }
+                    uint8_t* rowp = sl_ptr + lane * 128;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h < halves) {
+                    for (int j = 0; j < 8; ++j) {
+                        uint4* cell = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                        uint4 w;
+                        if (f32) {
+                            float v0 = __uint_as_float(r[4 * j]), v1 = __uint_as_float(r[4 * j + 1]);
+                            float v2 = __uint_as_float(r[4 * j + 2]), v3 = __uint_as_float(r[4 * j + 3]);
+                            if (p.has_c) {
+                                const float4 cv = *reinterpret_cast<const float4*>(cell);
+                                v0 += cv.x; v1 += cv.y; v2 += cv.z; v3 += cv.w;
+                            }
+                            w = make_uint4(__float_as_uint(v0), __float_as_uint(v1), __float_as_uint(v2),
+                                           __float_as_uint(v3));
+                        } else {
+                            uint32_t pk[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                const float4 cv = *reinterpret_cast<const float4*>(cp + h * 16 + i * 4);
-                                v[h * 16 + i * 4 + 0] += cv.x;
-                                v[h * 16 + i * 4 + 1] += cv.y;
-                                v[h * 16 + i * 4 + 2] += cv.z;
-                                v[h * 16 + i * 4 + 3] += cv.w;
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
+                                                                                __uint_as_float(r[8 * j + 2 * i + 1]));
+                                pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                            }
+                            w = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                        *cell = w;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kg) tma_store_3d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
+                        else tma_store_2d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32);
+                        bulk_commit_group();
+                        if (C::kSlots > 1 && p.has_c && c_have) {
+                            // refill the slot used by the previous chunk, once its store has read it
+                            bulk_wait_group_read<1>();
+                            issue_c(c_issued++);
+                        }
+                    }
+                } else {
+                    // Partially valid row group (no C in these layouts) or a chunk reaching past
+                    // the tile: per-thread stores of the valid rows and columns.  Drain the slot
+                    // stores first so the slot accounting above stays conservative.
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+                    if (row_ok) {
+                        const int left = ncols - c0;
+                        if (f32) {
+                            float* dp = static_cast<float*>(p.d) + grow * p.N + tl.n0 + c0;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (4 * j < left)
+                                    *reinterpret_cast<uint4*>(dp + 4 * j) =
+                                        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                        } else {
+                            __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.d) + grow * p.N + tl.n0 + c0;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (8 * j < left) {
+                                    uint32_t pk[4];
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                            __uint_as_float(r[8 * j + 2 * i]), __uint_as_float(r[8 * j + 2 * i + 1]));
+                                        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                                    }
+                                    *reinterpret_cast<uint4*>(dp + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                                }
                             }
                         }
                     }
                 }
-                if (p.d_f32) {
-                    float* dp = static_cast<float*>(p.d) + grow * p.N + n;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h < halves) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                *reinterpret_cast<float4*>(dp + h * 16 + i * 4) =
-                                    make_float4(v[h * 16 + i * 4], v[h * 16 + i * 4 + 1],
-                                                v[h * 16 + i * 4 + 2], v[h * 16 + i * 4 + 3]);
-                        }
-                    }
-                } else {
-                    __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.d) + grow * p.N + n;
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                        w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                    }
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (h < halves) {
-#pragma unroll
-                            for (int i = 0; i < 2; ++i)
-                                *reinterpret_cast<uint4*>(dp + h * 16 + i * 8) =
-                                    make_uint4(w[h * 8 + i * 4], w[h * 8 + i * 4 + 1],
-                                               w[h * 8 + i * 4 + 2], w[h * 8 + i * 4 + 3]);
-                        }
-                    }
-                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(acc));
+            if (aborted) break;
             if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
         }
+        if (lane == 0) {
+            // C loads issued but never consumed (abort) must land before the CTA exits.
+            for (uint32_t c = chunk_id; c < c_issued; ++c)
+                drain_bar(cfull_bar(ew, static_cast<int>(c % C::kSlots)), (c / C::kSlots) & 1u, 20000000ull);
+            bulk_wait_group<0>();
+        }
+        __syncwarp();
     }
 
     // ---------------------------------------------------------------- teardown

@@ -3,7 +3,9 @@
 #include "fg_gemm_inst.cuh"
 
 namespace fg {
-template cudaError_t launch_gemm<64, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<128, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<256, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<64, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<128, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<192, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<224, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 }  // namespace fg

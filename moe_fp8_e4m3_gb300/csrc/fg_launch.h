@@ -12,6 +12,6 @@ namespace fg {
 // Launches fg_gemm_kernel<BN, kTN> with `grid` persistent CTAs on `stream`.
 template <int BN, bool kTN>
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        int grid, cudaStream_t stream);
+                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream);
 
 }  // namespace fg

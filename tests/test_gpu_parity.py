@@ -56,12 +56,36 @@ def test_dense_parity(fg, m, n, k, with_c, out):
     C.compare(got.values(), C.dense_ref(case), f"dense {m}x{n}x{k}")
 
 
-@pytest.mark.parametrize("bn", ["64", "128", "256"])
-def test_dense_every_tile_width(fg, bn, monkeypatch):
+@pytest.mark.parametrize("bn", ["64", "128", "192", "224", "256"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_dense_every_tile_width(fg, bn, out, monkeypatch):
     monkeypatch.setenv("FG_FORCE_BN", bn)
-    case = C.dense_case(7, 256, 768, 512, True, "f32")
+    case = C.dense_case(7, 300, 784, 1024, out == "f32", out)   # ragged M and N, several tiles each
     got = run_dense(fg, case)
-    C.compare(got.values(), C.dense_ref(case), f"BN={bn}")
+    C.compare(got.values(), C.dense_ref(case), f"BN={bn} {out}")
+
+
+@pytest.mark.parametrize("bn", ["64", "192", "224", "256"])
+def test_grouped_every_tile_width(fg, bn, monkeypatch):
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.contiguous_case(9, num_tokens=512, num_routed=16, topk=3, num_groups=5, n=448, k=256)
+    d = run_contiguous(fg, case)
+    ref, written = C.contiguous_ref(case)
+    assert np.array_equal(~d.is_sentinel(), written)
+    C.compare(d.values()[written], ref[written], f"contiguous BN={bn}")
+    mc = C.masked_case(10, num_groups=3, m_max=160, n=448, k=256, masked_m=[0, 97, 160])
+    _check_masked(mc, run_masked(fg, mc))
+
+
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_k_grouped_every_tile_width(fg, bn, monkeypatch):
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.k_grouped_case(11, num_groups=3, m=256, n=384, ks=[256, 128, 0])
+    d = run_k_grouped(fg, case)
+    ref = C.k_grouped_ref(case)
+    vals = d.values().reshape(case["g"], case["m"], case["n"])
+    for e in range(case["g"]):
+        C.compare(vals[e], ref[e], f"k-grouped BN={bn} group {e}")
 
 
 def test_dense_d_aliases_c(fg):
