@@ -19,9 +19,8 @@
 // Warp roles (224 threads):
 //   warp 0      TMA producer: A and B tiles into a ring of shared-memory stages
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
-//   warp 2      scale loader: packed UE8M0 words into the tcgen05.cp layout, one packed
-//               word ahead (the loads of the next word are in flight while the current
-//               one is written into up to four stages)
+//   warp 2      scale loader: packed UE8M0 words copied by cp.async into the tcgen05.cp
+//               layout of each stage, completion tracked by the stage's mbarrier
 //   warps 3..6  epilogue: TMEM -> registers, + C (TMA-prefetched into shared memory),
 //               -> BF16/FP32 -> swizzled shared-memory slot -> TMA store
 // Accumulators are double-buffered in TMEM when two fit next to the scale slots
@@ -242,32 +241,6 @@ struct TileIter {
     }
 };
 
-// Scale words of one packed word `kw` of one tile: 4 SFA words and 4 per 128-row SFB
-// atom for this lane (MN index j * 32 + lane of each atom).
-template <int BN, bool kTN>
-struct ScaleWords {
-    static constexpr int kAtoms = (BN + 127) / 128;
-    int a[4];
-    int b[kAtoms][4];
-    __device__ __forceinline__ void load(const GemmParams& p, const Tile& tl, int kw, int lane) {
-        const int32_t* pa = p.sfa + tl.sfa_g * p.sfa_gstride + (long long)kw * p.sfa_ld;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int row = tl.sfa_row + lane + 32 * j;
-            a[j] = row < p.sfa_rows ? __ldg(pa + row) : 0;
-        }
-        const int32_t* pb = p.sfb + tl.g * p.sfb_gstride + (long long)kw * p.sfb_ld;
-#pragma unroll
-        for (int i = 0; i < kAtoms; ++i) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = tl.n0 + i * 128 + j * 32 + lane;
-                b[i][j] = n < p.N ? __ldg(pb + (kTN ? n : (n >> 7))) : 0;
-            }
-        }
-    }
-};
-
 template <int BN, bool kTN>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
@@ -296,7 +269,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full_bar(s), 2);     // producer arrive (+ TMA bytes) and scale loader
+            mbar_init(full_bar(s), 33);    // producer arrive (+ TMA bytes), 32 scale-loader lanes
             mbar_init(empty_bar(s), 1);    // tcgen05.commit of the MMA issuer
         }
         for (int b = 0; b < C::kNumAcc; ++b) {
@@ -428,6 +401,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                 const uint32_t d_t = tmem_base + acc * BN;
                 for (int kb = 0; kb < tl.nkb; ++kb) {
                     if (!wait_bar(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
+                    fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
                     tc_fence_after();
                     const uint32_t slot = kcount & 1u;
                     const uint32_t sfa_t = tmem_base + C::kSfCol0 + slot * 16;
@@ -472,57 +446,49 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         __syncwarp();
     } else if (warp == 2) {
         // ----------------------------------------------------- scale loader
-        // Units: (tile, packed word kw) covering up to four consecutive K-groups.  The
-        // words of the next unit are loaded while the current one fills its stages.
+        // Per stage: the packed UE8M0 word of its K-group for the tile's 128 A rows and BN
+        // B rows, copied with 4-byte cp.async straight into the tcgen05.cp layout (word
+        // (lane, j) of each 32x4 atom holds MN index j * 32 + lane; rows outside the
+        // problem are zero-filled).  Each lane's copies arrive on the stage's full barrier
+        // when they land, so this warp never waits for global-load latency.
         int s = 0;
         uint32_t ph = 0;
         TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
-        Tile tl, tn;
-        bool have = false;
-        while ((have = it.next(p, total_tiles, sched, cnt, tl)) && tl.nkb == 0) {
-        }
-        int kb = 0;
-        ScaleWords<BN, kTN> cur, nxt;
-        if (have) cur.load(p, tl, tl.kb0 >> 2, lane);
-        while (have) {
-            // the unit after the current one: same tile, next word; or the next tile's first
-            const int kw = (tl.kb0 + kb) >> 2;
-            const int kb_end = min(tl.nkb, (kw + 1) * 4 - tl.kb0);
-            bool have_next;
-            int next_kb;
-            if (kb_end < tl.nkb) {
-                tn = tl;
-                next_kb = kb_end;
-                have_next = true;
-            } else {
-                while ((have_next = it.next(p, total_tiles, sched, cnt, tn)) && tn.nkb == 0) {
-                }
-                next_kb = 0;
-            }
-            if (have_next) nxt.load(p, tn, (tn.kb0 + next_kb) >> 2, lane);
-            bool aborted = false;
-            for (; kb < kb_end; ++kb) {
+        Tile tl;
+        bool aborted = false;
+        while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
+            const int32_t* pa0 = p.sfa + tl.sfa_g * p.sfa_gstride;
+            const int32_t* pb0 = p.sfb + tl.g * p.sfb_gstride;
+            for (int kb = 0; kb < tl.nkb; ++kb) {
                 // warp-uniform decision: every lane leaves together on abort
                 const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                // word (lane, j) of each 32x4 atom holds MN index j * 32 + lane
-                *reinterpret_cast<int4*>(smem + C::kOffSfa + s * C::kSfaBytes + lane * 16) =
-                    make_int4(cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
+                const int kw = (tl.kb0 + kb) >> 2;
+                const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
+                const uint32_t da = sbase + C::kOffSfa + s * C::kSfaBytes + lane * 16;
 #pragma unroll
-                for (int i = 0; i < C::kSfbAtoms; ++i)
-                    *reinterpret_cast<int4*>(smem + C::kOffSfb + s * C::kSfbBytes + i * 512 + lane * 16) =
-                        make_int4(cur.b[i][0], cur.b[i][1], cur.b[i][2], cur.b[i][3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(s));
+                for (int j = 0; j < 4; ++j) {
+                    const int row = tl.sfa_row + lane + 32 * j;
+                    const bool in = row < p.sfa_rows;
+                    cp_async_4(da + 4 * j, in ? pa + row : pa, in ? 4u : 0u);
+                }
+                const int32_t* pb = pb0 + (long long)kw * p.sfb_ld;
+                const uint32_t db = sbase + C::kOffSfb + s * C::kSfbBytes + lane * 16;
+#pragma unroll
+                for (int i = 0; i < C::kSfbAtoms; ++i) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n = tl.n0 + i * 128 + j * 32 + lane;
+                        const bool in = n < p.N;
+                        cp_async_4(db + i * 512 + 4 * j, in ? pb + (kTN ? n : (n >> 7)) : pb, in ? 4u : 0u);
+                    }
+                }
+                cp_async_mbar_arrive(full_bar(s));
                 if (++s == C::kStages) { s = 0; ph ^= 1u; }
             }
-            if (aborted) break;
-            have = have_next;
-            tl = tn;
-            kb = next_kb;
-            cur = nxt;
         }
+        cp_async_wait_all();
+        __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM sub-partition this warp may read

@@ -81,6 +81,19 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+// 4-byte asynchronous global -> shared copy; src_bytes == 0 writes zeros (src unread).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared::cta.global [%0], [%1], 4, %2;"
+                 ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed (the
+// arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // reads (TMA stores, tcgen05.cp).
 __device__ __forceinline__ void fence_proxy_async_smem() {
