@@ -48,9 +48,10 @@ class GuardedOut:
 
     def values(self) -> np.ndarray:
         bits = self.inner_bits()
-        if self.out == "bf16":
-            return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        return bits.view(np.float32).astype(np.float64)
+        with np.errstate(invalid="ignore"):     # untouched rows hold a NaN sentinel
+            if self.out == "bf16":
+                return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            return bits.view(np.float32).astype(np.float64)
 
     def is_sentinel(self) -> np.ndarray:
         s = np.uint16(self.sentinel) if self.out == "bf16" else np.uint32(self.sentinel)

@@ -1,0 +1,110 @@
+"""GPU parity at the full benchmark sizes, in the launch configuration bench.py times
+(default tile choice, all SMs).  The oracle computes sampled output rows one by one;
+every row that must stay untouched is checked bit-exactly, and every output is checked
+finite."""
+import numpy as np
+import pytest
+
+import cases as C
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import moe_fp8_e4m3_gb300 as lib
+    return lib
+
+
+def _ok(fg):
+    st, detail = fg.get_device_error()
+    assert st == 0, (st, hex(detail))
+
+
+def _rows(m, n_samples, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    r = set(g.choice(m, size=min(m, n_samples), replace=False).tolist())
+    r |= {0, m - 1, min(127, m - 1), min(128, m - 1)}
+    return np.array(sorted(r))
+
+
+@pytest.mark.parametrize("m,n,k", [(4096, 7168, 2048), (64, 7168, 4096)])
+def test_dense_pair_full_size(fg, m, n, k):
+    from gpu_util import GuardedOut, dev
+    case = C.dense_case(1001, m, n, k, True, "f32")
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_gemm_nt(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), out.tensor,
+                   c=dev(case["c"]))
+    _ok(fg)
+    out.check_guards()
+    got = out.values()
+    assert np.all(np.isfinite(got))
+    rows = _rows(m, 48, 5)
+    C.compare(got[rows], C.dense_ref(case, rows=rows), f"dense {m}x{n}x{k} sampled rows")
+
+
+def test_contiguous_full_size(fg):
+    from gpu_util import GuardedOut, dev
+    case = C.contiguous_case(1002)            # 8192 tokens, top-6 of 256, experts 0-31, N=K=4096
+    d = GuardedOut(case["m_total"], case["n"], "bf16")
+    fg.m_grouped_fp8_gemm_nt_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(case["m_indices"]), d.tensor)
+    _ok(fg)
+    d.check_guards()
+    written = case["m_indices"] >= 0
+    assert np.array_equal(~d.is_sentinel(), written), "padding rows written or valid rows missing"
+    vals = d.values()
+    assert np.all(np.isfinite(vals[written]))
+    valid_rows = np.nonzero(written)[0]
+    g = np.random.Generator(np.random.PCG64(6))
+    rows = np.sort(g.choice(valid_rows, size=48, replace=False))
+    ref, _ = C.contiguous_ref(case, rows=rows)
+    C.compare(vals[rows], ref, "contiguous sampled rows")
+
+
+def test_masked_full_size(fg):
+    from gpu_util import GuardedOut, dev
+    case = C.masked_case(1003)                # 32 experts x 256 rows, N=4096, K=2048
+    g_, m_max, n = case["g"], case["m_max"], case["n"]
+    d = GuardedOut(g_ * m_max, n, "bf16")
+    fg.m_grouped_fp8_gemm_nt_masked(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                    dev(case["masked_m"]), d.tensor.view(g_, m_max, n),
+                                    expected_m=int(np.mean(case["masked_m"])))
+    _ok(fg)
+    d.check_guards()
+    sent = d.is_sentinel().reshape(g_, m_max)
+    vals = d.values().reshape(g_, m_max, n)
+    for e in range(g_):
+        mm = int(case["masked_m"][e])
+        assert not sent[e, :mm].any() and sent[e, mm:].all(), f"group {e}: rows beyond the mask written"
+        assert np.all(np.isfinite(vals[e, :mm]))
+    experts = [int(x) for x in np.argsort(case["masked_m"])[-3:]] + [int(np.argmin(np.where(case["masked_m"] > 0, case["masked_m"], 999)))]
+    ref = C.masked_ref(case, experts=experts)
+    for e in experts:
+        C.compare(vals[e, :int(case["masked_m"][e])], ref[e], f"masked group {e}")
+
+
+@pytest.mark.parametrize("alias", [False, True])
+def test_k_grouped_full_size(fg, alias):
+    from gpu_util import GuardedOut, dev
+    case = C.k_grouped_case(1004)             # 8 experts, M=4096, N=2048, sum K = 16384 (padded)
+    g_, m, n = case["g"], case["m"], case["n"]
+    d = GuardedOut(g_ * m, n, "f32")
+    if alias:
+        d.fill_from(case["c"].reshape(g_ * m, n))
+        c_t = d.tensor.view(g_, m, n)
+    else:
+        c_t = dev(case["c"])
+    fg.k_grouped_fp8_gemm_tn_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(case["ks"]), d.tensor.view(g_, m, n), c=c_t)
+    _ok(fg)
+    d.check_guards()
+    vals = d.values().reshape(g_, m, n)
+    assert np.all(np.isfinite(vals))
+    rows = _rows(m, 12, 7)
+    ref = C.k_grouped_ref(case, rows=rows)
+    for e in range(g_):
+        C.compare(vals[e][rows], ref[e], f"k-grouped group {e} sampled rows")
