@@ -117,7 +117,7 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G,
  *   d         [G][M_max][N] BF16 or FP32
  * Rows m >= masked_m[g] are never written, and their A rows (which may hold any bytes,
  * NaN codes included) never reach a valid row.  A mask outside [0, M_max] is clamped
- * and recorded as a device contract violation.  1 <= G <= 512, M_max >= 1.  No C operand.
+ * and recorded as a device contract violation.  1 <= G <= 256, M_max >= 1.  No C operand.
  */
 int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K,
                                     const uint8_t* a, const int32_t* sfa,
@@ -140,7 +140,7 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K,
  * Scale groups are counted over the concatenated K axis (group of element k is k/128),
  * so no group straddles two segments.  A ks that breaks these rules is a device
  * contract violation: nothing is written and the status word is set.
- * 1 <= G <= 512, K_total % 128 == 0, M >= 16 and M % 16 == 0, N % 16 == 0.
+ * 1 <= G <= 256, K_total % 128 == 0, M >= 16 and M % 16 == 0, N % 16 == 0.
  */
 int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total,
                                         const uint8_t* a, const int32_t* sfa,

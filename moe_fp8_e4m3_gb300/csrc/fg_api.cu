@@ -165,6 +165,27 @@ void fill_common(GemmParams& p, const DeviceState& st) {
     p.debug_stall = g_debug_stall;
 }
 
+int launch_nt_pair(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+                   const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
+    cudaError_t e;
+    switch (bn) {
+        case 128: e = fg::launch_gemm<128, false, true>(p, ma, mb, mc, md, grid, s); break;
+        case 224: e = fg::launch_gemm<224, false, true>(p, ma, mb, mc, md, grid, s); break;
+        default: e = fg::launch_gemm<256, false, true>(p, ma, mb, mc, md, grid, s); break;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    return FG_OK;
+}
+
+// CTA-pair (2-SM MMA) path for the dense GEMM: FG_2SM=1 forces it, FG_2SM=0 disables it.
+int use_pair_mode() {
+    const char* e = std::getenv("FG_2SM");
+    return e && e[0] == '1';
+}
+
 int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
               const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
     cudaError_t e;
@@ -220,12 +241,15 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
-    const int bn = choose_bn_nt(num_mb, N, sms, c != nullptr);
+    const bool pair = use_pair_mode() && num_mb >= 2 && sms >= 2;
+    int bn = choose_bn_nt(num_mb, N, sms, c != nullptr);
+    if (pair) bn = (bn == 256 || bn == 224 || bn == 128) ? bn : 224;
     GemmParams p{};
     p.kind = fg::kDense;
     p.M = M; p.N = N; p.K = K; p.G = 1;
     p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
-    p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
+    p.num_mb = pair ? ceil_div(num_mb, 2) : num_mb;   // pair mode: pairs of 128-row blocks
+    p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
     p.sfa_rows = M;
@@ -234,13 +258,16 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     CUtensorMap ma, mb, mc, md;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, pair ? bn / 2 : bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
-    const int grid = (int)(tiles < sms ? tiles : sms);
+    const int units = pair ? sms / 2 : sms;
+    const int grid = (int)(tiles < units ? tiles : units) * (pair ? 2 : 1);
     if (print_configs())
-        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d tiles=%lld grid=%d\n", M, N, K, bn, tiles, grid);
+        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d tiles=%lld grid=%d%s\n", M, N, K, bn, tiles, grid,
+                     pair ? " (CTA pairs)" : "");
+    if (pair) return launch_nt_pair(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 

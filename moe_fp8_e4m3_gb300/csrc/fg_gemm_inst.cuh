@@ -8,11 +8,11 @@
 
 namespace fg {
 
-template <int BN, bool kTN>
+template <int BN, bool kTN, bool k2Sm>
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
                         const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream) {
-    constexpr int kSmem = TileCfg<BN>::kSmemBytes;
-    auto kernel = fg_gemm_kernel<BN, kTN>;
+    constexpr int kSmem = TileCfg<BN, k2Sm>::kSmemBytes;
+    auto kernel = fg_gemm_kernel<BN, kTN, k2Sm>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -32,6 +32,15 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUt
     cfg.blockDim = dim3(224);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (k2Sm) {   // CTA pairs: grid is even, clusters of two along x
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, kernel, p, map_a, map_b, map_c, map_d);
 }
 

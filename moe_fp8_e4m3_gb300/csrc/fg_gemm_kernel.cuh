@@ -55,7 +55,7 @@ enum : int {
     kWaitEpilogueC = 6,
 };
 
-constexpr int kMaxGroups = 512;   // masked / K-grouped groups held in shared memory
+constexpr int kMaxGroups = 256;   // masked / K-grouped groups held in shared memory
 constexpr int kSmemLimit = 232448;
 
 struct GemmParams {
@@ -78,7 +78,7 @@ struct GemmParams {
     int debug_stall;
 };
 
-template <int BN>
+template <int BN, bool k2Sm = false>
 struct TileCfg {
     static constexpr int kBM = 128, kBK = 128;
     static constexpr int kSfbAtoms = (BN + 127) / 128;
@@ -87,12 +87,15 @@ struct TileCfg {
     static constexpr int kSfCol0 = (kNumAcc * BN + 15) / 16 * 16;
     static_assert(kSfCol0 + 16 + kSfCols <= 512, "TMEM columns");
     static constexpr int kABytes = kBM * kBK;              // 16 KB
-    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kBRows = k2Sm ? BN / 2 : BN;       // B rows held by this CTA
+    static constexpr int kBBytes = kBRows * kBK;
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = kSfbAtoms * 512;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     // Epilogue: per warp, kSlots shared-memory slots of 32 rows x 128 bytes.
-    static constexpr int kSlots = BN >= 256 ? 1 : 4;
+    // C-prefetch depth against pipeline stages: wide tiles keep four slots per warp (their
+    // epilogue streams the most C), narrow tiles and CTA pairs take more stages instead.
+    static constexpr int kSlots = k2Sm ? 2 : (BN >= 256 ? 1 : (BN >= 192 ? 4 : 2));
     static constexpr int kSlotBytes = 4096;
     static constexpr int kEpiBytes = 4 * kSlots * kSlotBytes;
     static constexpr int kMiscBytes = 1024 + 2 * (kMaxGroups + 1) * 4;   // barriers etc. + group tables
@@ -138,11 +141,17 @@ struct WaitCtl {
 
 // Bounded mbarrier wait.  Returns false if the CTA is aborting (flag raised here or
 // by another role).
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+// kCluster: the barrier is also arrived on from the paired CTA (acquire at cluster scope).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_scoped<kCluster>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait_scoped<kCluster>(bar, parity)) return true;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort = 1;
@@ -159,9 +168,11 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// In CTA-pair mode (dense only) a tile index names a pair of 128-row blocks; `rank`
+// selects this CTA's block and its half of the B rows.
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const int* sched,
-                                            const int* cnt, int& cursor) {
+                                            const int* cnt, int& cursor, int rank, bool pair) {
     Tile tl;
     tl.skip = false;
     tl.g = 0;
@@ -170,10 +181,11 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
     tl.sfa_g = 0;
     tl.d_z = 0;
     if (p.kind == kDense) {
-        const int mb = t % p.num_mb, nb = t / p.num_mb;
+        const int mbq = t % p.num_mb, nb = t / p.num_mb;
+        const int mb = pair ? 2 * mbq + rank : mbq;
         tl.n0 = nb * BN;
         tl.a_coord = mb * 128;
-        tl.b_coord = tl.n0;
+        tl.b_coord = pair ? tl.n0 + rank * (BN / 2) : tl.n0;
         tl.valid_rows = min(128, p.M - mb * 128);
         tl.d_row = mb * 128;
         tl.sfa_row = mb * 128;
@@ -230,27 +242,41 @@ template <int BN>
 struct TileIter {
     int t;
     int cursor;
+    int stride;
+    int rank;
+    bool pair;
     __device__ __forceinline__ bool next(const GemmParams& p, int total, const int* sched, const int* cnt,
                                          Tile& tl) {
         while (t < total) {
-            tl = decode_tile<BN>(p, t, sched, cnt, cursor);
-            t += gridDim.x;
+            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair);
+            t += stride;
             if (!tl.skip) return true;
         }
         return false;
     }
 };
 
-template <int BN, bool kTN>
+// Tiles of this CTA: blockIdx.x + i * gridDim.x, or per CTA pair in pair mode.
+template <int BN, bool k2Sm>
+__device__ __forceinline__ TileIter<BN> tiles_of_cta(int rank) {
+    if (k2Sm) return TileIter<BN>{static_cast<int>(blockIdx.x >> 1), 0, static_cast<int>(gridDim.x >> 1), rank, true};
+    return TileIter<BN>{static_cast<int>(blockIdx.x), 0, static_cast<int>(gridDim.x), 0, false};
+}
+
+template <int BN, bool kTN, bool k2Sm>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_d) {
-    using C = TileCfg<BN>;
+    static_assert(!(kTN && k2Sm), "CTA pairs are used by the NT kernels only");
+    using C = TileCfg<BN, k2Sm>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA pair: rank 0 (leader) issues the MMAs for both CTAs; rank 1 holds the other 128 rows.
+    const int rank = k2Sm ? static_cast<int>(cluster_ctarank()) : 0;
+    const bool leader = rank == 0;
 
     const uint32_t bar0 = sbase + C::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -269,12 +295,15 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full_bar(s), 33);    // producer arrive (+ TMA bytes), 32 scale-loader lanes
+            // producer arrive (+ TMA bytes of both CTAs in pair mode), 32 scale-loader lanes,
+            // and in pair mode the peer's scale relay; the peer's own barrier counts only
+            // its scale-loader lanes.
+            mbar_init(full_bar(s), k2Sm ? (leader ? 34 : 32) : 33);
             mbar_init(empty_bar(s), 1);    // tcgen05.commit of the MMA issuer
         }
         for (int b = 0; b < C::kNumAcc; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);     // one arrive per epilogue warp
+            mbar_init(acce_bar(b), k2Sm && leader ? 8 : 4);   // one arrive per epilogue warp (of both CTAs)
         }
         mbar_init(mma_drain_bar, 1);
         for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
@@ -329,11 +358,17 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
+        if constexpr (k2Sm) {   // collective: one warp of each CTA of the pair
+            tmem_alloc_pair(smem_u32(tmem_slot), 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), 512);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (k2Sm) cluster_sync();   // the pair's barriers are initialised before either CTA uses them
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (p.kind == kMasked) total_tiles = sched[p.G];
@@ -346,10 +381,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            bool stall = p.debug_stall != 0;
+            bool stall = p.debug_stall != 0 && leader;
             uint32_t armed = 0, armed_par = 0;   // per-stage: armed at least once / parity
             bool aborted = false;
-            TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
             Tile tl;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
                 for (int kb = 0; kb < tl.nkb; ++kb) {
@@ -358,14 +393,21 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                         stall = false;   // leave this stage unarmed: the MMA issuer times out
                     } else {
                         const uint32_t fb = full_bar(s);
-                        mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
                         const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
                         const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
                         const int kc = (tl.kb0 + kb) * 128;
-                        if (!kTN) {
+                        if constexpr (k2Sm) {
+                            // both CTAs' tiles complete on the leader's barrier
+                            if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kABytes + C::kBBytes));
+                            const uint32_t fbl = map_shared_rank(fb, 0);
+                            tma_load_2d_pair(sa, &tm_a, fbl, kc, tl.a_coord);
+                            tma_load_2d_pair(sb, &tm_b, fbl, kc, tl.b_coord);
+                        } else if (!kTN) {
+                            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
                             tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
                         } else {
+                            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
                             tma_load_2d(sa, &tm_a, fb, tl.a_coord, kc);
 #pragma unroll
                             for (int h = 0; h < BN / 128; ++h)
@@ -377,7 +419,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (aborted || *abort_flag) {
+            if (leader && (aborted || *abort_flag)) {
                 // Bounded drain of loads that may still be landing in shared memory.
                 for (int i = 0; i < C::kStages; ++i)
                     if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
@@ -385,22 +427,39 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdesc = make_idesc_mxf8(128, BN, kTN, kTN);
+        if (lane == 0 && k2Sm && !leader) {
+            // Peer of a CTA pair: the leader's MMAs read this CTA's shared memory, so the
+            // leader must learn when this CTA's scale words have landed: relay each stage's
+            // completion (local barrier, 32 scale-loader lanes) to the leader's stage barrier.
+            int s = 0;
+            uint32_t ph = 0;
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+            Tile tl;
+            bool aborted = false;
+            while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
+                for (int kb = 0; kb < tl.nkb; ++kb) {
+                    if (!wait_bar(full_bar(s), ph, wctl, kWaitScales)) { aborted = true; break; }
+                    fence_proxy_async_smem();
+                    mbar_arrive_remote(map_shared_rank(full_bar(s), 0));
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                }
+            }
+        } else if (lane == 0) {
+            constexpr uint32_t kIdesc = make_idesc_mxf8(k2Sm ? 256 : 128, BN, kTN, kTN);
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
             uint32_t kcount = 0;
             bool aborted = false;
-            TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
             Tile tl;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
-                if (!wait_bar(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
+                if (!wait_bar<k2Sm>(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_t = tmem_base + acc * BN;
                 for (int kb = 0; kb < tl.nkb; ++kb) {
-                    if (!wait_bar(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
+                    if (!wait_bar<k2Sm>(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
                     fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
                     tc_fence_after();
                     const uint32_t slot = kcount & 1u;
@@ -408,10 +467,14 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     const uint32_t sfb_t = sfa_t + 4;
                     const uint32_t ssfa = sbase + C::kOffSfa + s * C::kSfaBytes;
                     const uint32_t ssfb = sbase + C::kOffSfb + s * C::kSfbBytes;
-                    tc_cp_32x128b_warpx4(sfa_t, make_sdesc(ssfa, 0, 128, kLayoutNone));
+                    // pair mode: each CTA's scale words go from its shared memory to its TMEM
+                    if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_t, make_sdesc(ssfa, 0, 128, kLayoutNone));
+                    else tc_cp_32x128b_warpx4(sfa_t, make_sdesc(ssfa, 0, 128, kLayoutNone));
 #pragma unroll
-                    for (int i = 0; i < C::kSfbAtoms; ++i)
-                        tc_cp_32x128b_warpx4(sfb_t + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
+                    for (int i = 0; i < C::kSfbAtoms; ++i) {
+                        if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfb_t + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
+                        else tc_cp_32x128b_warpx4(sfb_t + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
+                    }
                     const uint32_t sf_id = static_cast<uint32_t>(tl.kb0 + kb) & 3u;
                     const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, sf_id);
                     const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
@@ -426,18 +489,23 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                             ad = make_sdesc(sa + 4096 * j, 16384, 1024, kLayoutSw128);
                             bd = make_sdesc(sb + 4096 * j, 16384, 1024, kLayoutSw128);
                         }
-                        tc_mma_mxf8(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
+                        if constexpr (k2Sm) tc_mma_mxf8_pair(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
+                        else tc_mma_mxf8(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
                     }
-                    tc_commit(empty_bar(s));
+                    if constexpr (k2Sm) tc_commit_pair_multicast(empty_bar(s));   // frees the stage in both CTAs
+                    else tc_commit(empty_bar(s));
                     ++kcount;
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
                 if (aborted) break;
-                if (tl.nkb > 0) tc_commit(accf_bar(acc)); else mbar_arrive(accf_bar(acc));
+                if constexpr (k2Sm) tc_commit_pair_multicast(accf_bar(acc));   // dense: every tile has K-blocks
+                else if (tl.nkb > 0) tc_commit(accf_bar(acc));
+                else mbar_arrive(accf_bar(acc));
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
             // Wait (bounded) until every tensor-core operation issued here has finished.
-            tc_commit(mma_drain_bar);
+            if constexpr (k2Sm) tc_commit_pair_local(mma_drain_bar);
+            else tc_commit(mma_drain_bar);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(mma_drain_bar, 0)) {
                 if (globaltimer_ns() - t0 > p.timeout_ns) { record_status(p.status, kErrTimeout | kWaitDrain); break; }
@@ -453,7 +521,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         // when they land, so this warp never waits for global-load latency.
         int s = 0;
         uint32_t ph = 0;
-        TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
         Tile tl;
         bool aborted = false;
         while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
@@ -501,7 +569,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         const bool kg = p.kind == kKGrouped;
 
         // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
-        TileIter<BN> cit{static_cast<int>(blockIdx.x), 0};
+        TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank);
         Tile ctl;
         bool c_have = p.has_c ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
         int c_chunk = 0;
@@ -530,11 +598,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         uint32_t acc_ph = 0;
         uint32_t chunk_id = 0;       // chunks consumed so far
         bool aborted = false;
-        TileIter<BN> it{static_cast<int>(blockIdx.x), 0};
+        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
         Tile tl;
         while (it.next(p, total_tiles, sched, cnt, tl)) {
             // warp-uniform decision before the .sync.aligned TMEM loads below
-            const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+            const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
             if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
             tc_fence_after();
             const long long grow = tl.d_row + row;
@@ -574,7 +642,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     // the accumulator buffer is free once its last columns are in registers
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                    if (lane == 0) {
+                        if (k2Sm && !leader) mbar_arrive_remote(map_shared_rank(acce_bar(acc), 0));
+                        else mbar_arrive(acce_bar(acc));
+                    }
                 }
                 // A 64-column BF16 chunk at the end of a BN = 224 tile would store into the
                 // neighbouring tile: such a chunk takes the per-thread path (no C in BF16).
@@ -682,10 +753,12 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    __syncthreads();
+    if constexpr (k2Sm) cluster_sync();   // the leader's MMAs may use this CTA's memory until here
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 512);
+        if constexpr (k2Sm) tmem_dealloc_pair(tmem_base, 512);
+        else tmem_dealloc(tmem_base, 512);
     }
 }
 

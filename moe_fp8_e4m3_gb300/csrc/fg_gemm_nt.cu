@@ -8,4 +8,8 @@ template cudaError_t launch_gemm<128, false>(const GemmParams&, const CUtensorMa
 template cudaError_t launch_gemm<192, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 template cudaError_t launch_gemm<224, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 template cudaError_t launch_gemm<256, false>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+// CTA-pair variants (dense)
+template cudaError_t launch_gemm<128, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<224, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 }  // namespace fg

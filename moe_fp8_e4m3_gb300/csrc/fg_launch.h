@@ -9,8 +9,9 @@
 
 namespace fg {
 
-// Launches fg_gemm_kernel<BN, kTN> with `grid` persistent CTAs on `stream`.
-template <int BN, bool kTN>
+// Launches fg_gemm_kernel<BN, kTN, k2Sm> with `grid` persistent CTAs on `stream`.
+// k2Sm: clusters of two CTAs sharing one 256-row MMA (dense NT only).
+template <int BN, bool kTN, bool k2Sm = false>
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
                         const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream);
 

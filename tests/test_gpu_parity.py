@@ -280,3 +280,33 @@ def test_k_grouped_bad_segments_reported(fg):
     st, detail = fg.get_device_error()
     assert st == fg.FG_ERR_DEVICE_CONTRACT and detail == 0x104
     assert np.all(d.is_sentinel())
+
+
+# ------------------------------------------------------- CTA-pair (2-SM) path
+@pytest.mark.parametrize("bn", ["128", "224", "256"])
+def test_dense_cta_pairs(fg, bn, monkeypatch):
+    """The opt-in 2-SM MMA path (FG_2SM=1): one 256-row MMA per CTA pair, each CTA
+    holding half of B.  Odd number of 128-row blocks (the last pair is half empty),
+    ragged N, and C aliasing D."""
+    monkeypatch.setenv("FG_2SM", "1")
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.dense_case(61, 3 * 128 + 40, 800, 768, True, "f32")
+    C.compare(run_dense(fg, case).values(), C.dense_ref(case), f"pairs BN={bn}")
+    C.compare(run_dense(fg, case, alias_c=True).values(), C.dense_ref(case), f"pairs BN={bn} aliased")
+
+
+def test_scale_probe_cta_pairs(fg, monkeypatch):
+    from gpu_util import GuardedOut, dev
+    monkeypatch.setenv("FG_2SM", "1")
+    m, n, groups = 512, 448, 8
+    ea, eb = P.scale_probe_inputs(m, n, groups)
+    a = np.full((m, groups * 128), 0x38, np.uint8)
+    b = np.full((n, groups * 128), 0x38, np.uint8)
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_gemm_nt(dev(a), dev(F.pack_ue8m0((ea + 127).astype(np.uint8))), dev(b),
+                   dev(F.pack_ue8m0((eb + 127).astype(np.uint8))), out.tensor)
+    _status_ok(fg)
+    want = np.zeros((m, n))
+    for gg in range(groups):
+        want += 2.0 ** (7 + ea[:, gg][:, None] + eb[np.arange(n) // 128, gg][None, :])
+    assert np.array_equal(out.values(), want)
