@@ -192,6 +192,16 @@ int fg_get_tma_aligned_size(int x, int elem_bytes);
 void fg_set_num_sms(int n);
 int fg_get_num_sms(void);
 
+/* Programmatic dependent launch of the GEMM kernels (section 10, set_pdl/get_pdl).
+ * Enabled (the default), every GEMM is launched so that it may begin while the previous
+ * kernel of the stream is still finishing: its CTAs initialise barriers and tensor
+ * memory, then wait until the previous grid has completed and its writes are visible
+ * before touching global memory (so results never depend on the setting); and each GEMM
+ * allows the next programmatic launch to begin as soon as all of its CTAs are running.
+ * enable = 0 launches with plain stream ordering. */
+void fg_set_pdl(int enable);
+int fg_get_pdl(void);
+
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: FG_OK, FG_ERR_DEVICE_CONTRACT or FG_ERR_DEVICE_TIMEOUT (first event
  * since the last read), or FG_ERR_CUDA if the synchronisation itself failed.

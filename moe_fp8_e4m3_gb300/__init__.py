@@ -37,6 +37,8 @@ _SIGNATURES = {
     "fg_get_tma_aligned_size": (_I, [_I, _I]),
     "fg_set_num_sms": (None, [_I]),
     "fg_get_num_sms": (_I, []),
+    "fg_set_pdl": (None, [_I]),
+    "fg_get_pdl": (_I, []),
     "fg_get_device_error": (_I, [_P, ctypes.POINTER(_I)]),
     "fg_status_string": (ctypes.c_char_p, [_I]),
     "fg_debug_inject_stall": (None, [_I, ctypes.c_uint32]),
@@ -200,6 +202,15 @@ def set_num_sms(n: int) -> None:
 
 def get_num_sms() -> int:
     return lib.fg_get_num_sms()
+
+
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch of the GEMM kernels on (default) or off."""
+    lib.fg_set_pdl(1 if enable else 0)
+
+
+def get_pdl() -> bool:
+    return bool(lib.fg_get_pdl())
 
 
 def get_device_error(stream=None) -> tuple[int, int]:

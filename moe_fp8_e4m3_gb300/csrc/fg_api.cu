@@ -25,10 +25,15 @@ using fg::GemmParams;
 constexpr int kMaxDevices = 256;
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;  // 4 s per wait
 
+constexpr int kBnChoices[5] = {64, 128, 192, 224, 256};
+
 struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     int* status = nullptr;
+    // resident clusters of the dense NT kernel per tile width and cluster size 2/4/8
+    // (index 3: CTA pairs of the 2-SM kernel); 0 = not queried yet, -1 = query failed
+    int clusters[5][4] = {};
 };
 
 std::mutex g_mu;
@@ -37,6 +42,7 @@ int g_num_sms_limit = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
 int g_debug_stall = 0;
+int g_pdl = 1;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 
 int device_state(DeviceState** out) {
@@ -79,6 +85,42 @@ int device_state(DeviceState** out) {
 
 int sms_in_use(const DeviceState& st) {
     return (g_num_sms_limit > 0 && g_num_sms_limit < st.num_sms) ? g_num_sms_limit : st.num_sms;
+}
+
+// Clusters of `cluster` CTAs (2, 4 or 8; pair: the 2-SM kernel) that fit on the device at once.
+int resident_clusters(DeviceState& st, int bn, int cluster, bool pair) {
+    int bi = 0;
+    while (bi < 4 && kBnChoices[bi] != bn) ++bi;
+    const int ci = pair ? 3 : (cluster == 2 ? 0 : (cluster == 4 ? 1 : 2));
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (st.clusters[bi][ci] != 0) return st.clusters[bi][ci] > 0 ? st.clusters[bi][ci] : 0;
+    }
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (pair) {
+        switch (bn) {
+            case 128: e = fg::max_active_clusters<128, false, true>(2, &n); break;
+            case 224: e = fg::max_active_clusters<224, false, true>(2, &n); break;
+            case 256: e = fg::max_active_clusters<256, false, true>(2, &n); break;
+            default: break;
+        }
+    } else {
+        switch (bn) {
+            case 64: e = fg::max_active_clusters<64, false, false, true>(cluster, &n); break;
+            case 128: e = fg::max_active_clusters<128, false, false, true>(cluster, &n); break;
+            case 192: e = fg::max_active_clusters<192, false, false, true>(cluster, &n); break;
+            case 224: e = fg::max_active_clusters<224, false, false, true>(cluster, &n); break;
+            default: e = fg::max_active_clusters<256, false, false, true>(cluster, &n); break;
+        }
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        n = -1;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    st.clusters[bi][ci] = n;
+    return n > 0 ? n : 0;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -127,9 +169,17 @@ bool print_configs() {
     return e && e[0] == '1';
 }
 
-// Optional override of the N tile (tuning aid): FG_FORCE_BN=64|128|256.
+// Optional override of the N tile (tuning aid): FG_FORCE_BN=64|128|192|224|256.
 int forced_bn() {
     const char* e = std::getenv("FG_FORCE_BN");
+    return e ? std::atoi(e) : 0;
+}
+
+// Optional override of the dense split-K cluster size (tuning aid): FG_FORCE_SPLIT=1|2|4|8.
+// A forced split that cannot run (too many tiles for one resident wave of clusters)
+// falls back to the model's choice.
+int forced_split() {
+    const char* e = std::getenv("FG_FORCE_SPLIT");
     return e ? std::atoi(e) : 0;
 }
 
@@ -152,6 +202,53 @@ int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     return best;
 }
 
+// Dense NT tiling: N tile and split-K cluster size.  Without a split the N tile is
+// choose_bn_nt's.  A split-K cluster of s CTAs needs every tile's cluster resident in one
+// wave; the choice between the two compares estimated times (microseconds):
+//     waves * ceil(nkb / s) * t_kb(BN) + t_x(s)
+// t_kb is the steady-state time of one K-group per CTA and t_x(s) the partial-tile
+// exchange plus cluster barriers, both measured on a 64 x 7168 x 4096 GEMM on GB300 with
+// all SMs busy and L2 flushed (TMA latency bound: deeper rings of narrow tiles keep up).
+double t_kb_us(int bn) {
+    switch (bn) {
+        case 64: return 0.36;
+        case 128: return 0.37;
+        case 192: return 0.50;
+        default: return 0.61;
+    }
+}
+double t_x_us(int s) { return s <= 1 ? 0.0 : (s == 2 ? 0.5 : (s == 4 ? 2.5 : 5.0)); }
+
+struct DenseTiling {
+    int bn;
+    int split;
+};
+DenseTiling choose_dense_tiling(DeviceState& st, int num_mb, int n, int k, int sms, bool has_c) {
+    const int fb = forced_bn(), fs = forced_split();
+    const int nkb = k / 128;
+    DenseTiling best{choose_bn_nt(num_mb, n, sms, has_c), 1};
+    const long long tiles1 = (long long)num_mb * ceil_div(n, best.bn);
+    double best_t = (double)((tiles1 + sms - 1) / sms) * nkb * t_kb_us(best.bn);
+    if (fs == 1) return best;
+    for (int bn : {256, 224, 192, 128, 64}) {
+        if (fb && bn != fb) continue;
+        const long long tiles = (long long)num_mb * ceil_div(n, bn);
+        for (int s : {2, 4, 8}) {
+            if (fs && s != fs) continue;
+            if (tiles * s > sms) continue;
+            if (!fs && nkb < 2 * s) continue;
+            if (tiles > resident_clusters(st, bn, s, false)) continue;
+            const double t = ceil_div(nkb, s) * t_kb_us(bn) + t_x_us(s);
+            if (fs || t < best_t) {
+                best = DenseTiling{bn, s};
+                best_t = t;
+                if (fs) return best;
+            }
+        }
+    }
+    return best;
+}
+
 int choose_bn_tn(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     const int f = forced_bn();
     if (f == 128 || f == 256) return f;
@@ -160,9 +257,12 @@ int choose_bn_tn(long long row_blocks, int n, int sms, bool heavy_epilogue) {
 }
 
 void fill_common(GemmParams& p, const DeviceState& st) {
+    p.split = 1;
+    p.a_box_rows = 128;
     p.status = st.status;
     p.timeout_ns = g_timeout_ns;
     p.debug_stall = g_debug_stall;
+    p.pdl = g_pdl;
 }
 
 int launch_nt_pair(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
@@ -189,6 +289,20 @@ int use_pair_mode() {
 int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
               const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
     cudaError_t e;
+    if (p.split > 1) {
+        switch (bn) {
+            case 64: e = fg::launch_gemm<64, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+            case 128: e = fg::launch_gemm<128, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+            case 192: e = fg::launch_gemm<192, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+            case 224: e = fg::launch_gemm<224, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+            default: e = fg::launch_gemm<256, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+        }
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return FG_ERR_CUDA;
+        }
+        return FG_OK;
+    }
     switch (bn) {
         case 64: e = fg::launch_gemm<64, false>(p, ma, mb, mc, md, grid, s); break;
         case 128: e = fg::launch_gemm<128, false>(p, ma, mb, mc, md, grid, s); break;
@@ -242,9 +356,16 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
     const bool pair = use_pair_mode() && num_mb >= 2 && sms >= 2;
-    int bn = choose_bn_nt(num_mb, N, sms, c != nullptr);
-    if (pair) bn = (bn == 256 || bn == 224 || bn == 128) ? bn : 224;
+    DenseTiling tiling{0, 1};
+    if (pair) {
+        const int b0 = choose_bn_nt(num_mb, N, sms, c != nullptr);
+        tiling.bn = (b0 == 256 || b0 == 224 || b0 == 128) ? b0 : 224;
+    } else {
+        tiling = choose_dense_tiling(*st, num_mb, N, K, sms, c != nullptr);
+    }
+    const int bn = tiling.bn;
     GemmParams p{};
+    fill_common(p, *st);
     p.kind = fg::kDense;
     p.M = M; p.N = N; p.K = K; p.G = 1;
     p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
@@ -254,19 +375,33 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
     p.sfa_rows = M;
     p.d = d;
-    fill_common(p, *st);
+    p.c = c;
+    p.split = tiling.split;
+    // a single row block of at most 64 rows: load only those rows of A (the MMA still
+    // reads 128 rows of shared memory; rows past M produce accumulator rows never stored)
+    p.a_box_rows = (!pair && M <= 64) ? 64 : 128;
     CUtensorMap ma, mb, mc, md;
     std::memset(&mc, 0, sizeof(mc));
-    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, pair ? bn / 2 : bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
-    const int units = pair ? sms / 2 : sms;
-    const int grid = (int)(tiles < units ? tiles : units) * (pair ? 2 : 1);
+    int grid;
+    if (pair) {
+        // whole pairs only, and no more pairs than can be resident at once
+        int units = sms / 2;
+        const int rc2 = resident_clusters(*st, bn, 2, true);
+        if (rc2 > 0 && rc2 < units) units = rc2;
+        grid = (int)(tiles < units ? tiles : units) * 2;
+    } else if (p.split > 1) {
+        grid = (int)tiles * p.split;    // one tile per cluster, all clusters resident
+    } else {
+        grid = (int)(tiles < sms ? tiles : sms);
+    }
     if (print_configs())
-        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d tiles=%lld grid=%d%s\n", M, N, K, bn, tiles, grid,
-                     pair ? " (CTA pairs)" : "");
+        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d%s\n", M, N, K, bn,
+                     p.split, tiles, grid, pair ? " (CTA pairs)" : "");
     if (pair) return launch_nt_pair(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -414,6 +549,16 @@ int fg_get_tma_aligned_size(int x, int elem_bytes) {
 void fg_set_num_sms(int n) {
     std::lock_guard<std::mutex> lock(g_mu);
     g_num_sms_limit = n > 0 ? n : 0;
+}
+
+void fg_set_pdl(int enable) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_pdl = enable ? 1 : 0;
+}
+
+int fg_get_pdl(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_pdl;
 }
 
 int fg_get_num_sms(void) {

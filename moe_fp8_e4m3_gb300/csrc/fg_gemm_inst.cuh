@@ -8,40 +8,71 @@
 
 namespace fg {
 
-template <int BN, bool kTN, bool k2Sm>
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream) {
+// Raises the kernel's dynamic shared-memory limit once per device.
+template <int BN, bool kTN, bool k2Sm, bool kSplit>
+cudaError_t configure_gemm() {
     constexpr int kSmem = TileCfg<BN, k2Sm>::kSmemBytes;
-    auto kernel = fg_gemm_kernel<BN, kTN, k2Sm>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     static std::mutex mu;
     static bool configured[256] = {};
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-        if (!configured[dev]) {
-            err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-            if (err != cudaSuccess) return err;
-            configured[dev] = true;
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        err = cudaFuncSetAttribute(fg_gemm_kernel<BN, kTN, k2Sm, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (err != cudaSuccess) return err;
+        configured[dev] = true;
     }
+    return cudaSuccess;
+}
+
+// Appends the launch attributes: clusters of `cluster` CTAs along x (cluster > 1) and
+// programmatic stream serialisation (pdl).  attr holds two entries.
+inline void set_launch_attrs(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int cluster, bool pdl) {
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
+}
+
+template <int BN, bool kTN, bool k2Sm, bool kSplit>
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream) {
+    cudaError_t err = configure_gemm<BN, kTN, k2Sm, kSplit>();
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(224);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm>::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (k2Sm) {   // CTA pairs: grid is even, clusters of two along x
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, kernel, p, map_a, map_b, map_c, map_d);
+    cudaLaunchAttribute attr[2];
+    set_launch_attrs(cfg, attr, k2Sm ? 2 : (kSplit ? p.split : 1), p.pdl != 0);
+    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kTN, k2Sm, kSplit>, p, map_a, map_b, map_c, map_d);
+}
+
+template <int BN, bool kTN, bool k2Sm, bool kSplit>
+cudaError_t max_active_clusters(int cluster, int* out) {
+    cudaError_t err = configure_gemm<BN, kTN, k2Sm, kSplit>();
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+    cfg.blockDim = dim3(224);
+    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm>::kSmemBytes;
+    cudaLaunchAttribute attr[2];
+    set_launch_attrs(cfg, attr, cluster, false);
+    return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kTN, k2Sm, kSplit>, &cfg);
 }
 
 }  // namespace fg

@@ -25,6 +25,11 @@
 //               -> BF16/FP32 -> swizzled shared-memory slot -> TMA store
 // Accumulators are double-buffered in TMEM when two fit next to the scale slots
 // (BN <= 224), so the epilogue of one tile overlaps the MMAs of the next.
+//
+// Split-K clusters (dense NT, few output tiles): a cluster of `split` CTAs shares one
+// output tile, each CTA runs a contiguous share of the K-groups, and the partial FP32
+// tiles are summed through distributed shared memory in rank order (deterministic),
+// each CTA reducing and storing one slice of the tile's columns.
 // Every role walks the same static persistent tile sequence (tile = blockIdx.x +
 // i * gridDim.x), decoded from device-resident segment data without host sync.
 //
@@ -51,8 +56,9 @@ enum : int {
     kChkMixedBlock = 2,        // a row names another group than its block
     kChkMaskRange = 3,         // masked_m outside [0, M_max]
     kChkKSegments = 4,         // ks not multiples of 128 / negative / wrong sum
+    kChkSplit = 5,             // split-K launch without one tile per cluster
     kWaitProducer = 1, kWaitMma = 2, kWaitScales = 3, kWaitEpilogue = 4, kWaitDrain = 5,
-    kWaitEpilogueC = 6,
+    kWaitEpilogueC = 6, kWaitExchange = 7,
 };
 
 constexpr int kMaxGroups = 256;   // masked / K-grouped groups held in shared memory
@@ -73,6 +79,10 @@ struct GemmParams {
     const int32_t* masked_m;
     const int32_t* ks;
     void* d;               // for the per-thread store path (partially valid row groups)
+    const float* c;        // C for the split-K reduction (nullable)
+    int split;             // CTAs per cluster sharing one tile along K (1: no split)
+    int a_box_rows;        // rows of the A tensor-map box (128, or 64 when every tile has <= 64 rows)
+    int pdl;               // host side: launch with programmatic stream serialisation
     int* status;
     unsigned long long timeout_ns;
     int debug_stall;
@@ -107,7 +117,7 @@ struct TileCfg {
     static constexpr int kOffSfa = kOffEpi + kEpiBytes;
     static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
     static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1 + 4 * kSlots;
+    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1 + 4 * kSlots + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;                   // tmem addr, abort flag
     static constexpr int kOffSched = kOffMisc + 16;                           // int[kMaxGroups + 1]
     static constexpr int kOffCnt = kOffSched + (kMaxGroups + 1) * 4;
@@ -116,6 +126,10 @@ struct TileCfg {
     static_assert(kStages >= 2, "pipeline depth");
     static_assert(kNumBars * 8 <= 1024 - 16, "barrier area");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    // Split-K exchange buffer: the FP32 partial tile, rows padded by 16 bytes, in the
+    // operand ring (idle once the cluster's single tile has been accumulated).
+    static constexpr int kXStride = BN + 4;
+    static_assert(kStages * (kABytes + kBBytes) >= kBM * kXStride * 4, "split-K exchange buffer");
 };
 
 struct Tile {
@@ -172,7 +186,7 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigne
 // selects this CTA's block and its half of the B rows.
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const int* sched,
-                                            const int* cnt, int& cursor, int rank, bool pair) {
+                                            const int* cnt, int& cursor, int rank, bool pair, int split) {
     Tile tl;
     tl.skip = false;
     tl.g = 0;
@@ -189,6 +203,11 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
         tl.valid_rows = min(128, p.M - mb * 128);
         tl.d_row = mb * 128;
         tl.sfa_row = mb * 128;
+        if (split > 1) {     // this CTA's share of the K-groups: [r*nkb/split, (r+1)*nkb/split)
+            const int nkb = tl.nkb;
+            tl.kb0 = rank * nkb / split;
+            tl.nkb = (rank + 1) * nkb / split - tl.kb0;
+        }
     } else if (p.kind == kContiguous) {
         const int mb = t / p.num_nb, nb = t % p.num_nb;
         const int g = __ldg(p.m_indices + (long long)mb * 128);
@@ -245,10 +264,11 @@ struct TileIter {
     int stride;
     int rank;
     bool pair;
+    int split;
     __device__ __forceinline__ bool next(const GemmParams& p, int total, const int* sched, const int* cnt,
                                          Tile& tl) {
         while (t < total) {
-            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair);
+            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair, split);
             t += stride;
             if (!tl.skip) return true;
         }
@@ -256,27 +276,149 @@ struct TileIter {
     }
 };
 
-// Tiles of this CTA: blockIdx.x + i * gridDim.x, or per CTA pair in pair mode.
+// Tiles of this CTA: blockIdx.x + i * gridDim.x, or per cluster (CTA pair, split-K
+// cluster) when clusters share tiles.
 template <int BN, bool k2Sm>
-__device__ __forceinline__ TileIter<BN> tiles_of_cta(int rank) {
-    if (k2Sm) return TileIter<BN>{static_cast<int>(blockIdx.x >> 1), 0, static_cast<int>(gridDim.x >> 1), rank, true};
-    return TileIter<BN>{static_cast<int>(blockIdx.x), 0, static_cast<int>(gridDim.x), 0, false};
+__device__ __forceinline__ TileIter<BN> tiles_of_cta(int rank, int split) {
+    if (k2Sm) return TileIter<BN>{static_cast<int>(blockIdx.x >> 1), 0, static_cast<int>(gridDim.x >> 1), rank, true, 1};
+    return TileIter<BN>{static_cast<int>(blockIdx.x) / split, 0, static_cast<int>(gridDim.x) / split, rank, false, split};
 }
 
-template <int BN, bool kTN, bool k2Sm>
+// ------------------------------------------------------------ split-K exchange
+// Epilogue of one tile shared by a split-K cluster (kept out of line: the common
+// epilogue path never fetches its code).
+//   1. the partial tile (TMEM) -> this CTA's exchange buffer, valid rows only;
+//   2. every epilogue warp of the cluster arrives on every CTA's exchange barrier;
+//   3. this CTA sums its column slice over the cluster's buffers in rank order
+//      (rank 0's value, + rank 1's, ...), adds C and stores D.
+// The teardown cluster barrier keeps each buffer alive until every peer has read it.
+// Returns false on abort (time-out).
+struct SplitTile {
+    int valid_rows, n0, N, nkb;
+    long long d_row;
+    int has_c, d_f32;
+    const float* c;
+    void* d;
+};
+
+template <int BN, class C>
+__device__ __noinline__ bool split_k_tile(const SplitTile st, float* xb, uint32_t tmem_acc, uint32_t accf,
+                                          uint32_t acc_ph, uint32_t acce, uint32_t xfull, uint32_t x_ph,
+                                          const WaitCtl wctl, int rank, int split) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;                                // TMEM sub-partition of this warp
+    const int row = q * 32 + lane;
+    const int te = static_cast<int>(threadIdx.x) - 96;     // 0..127 over the epilogue warps
+    constexpr int kB = 4;                                  // slice items (float4 groups) per thread and pass
+    const int vr = st.valid_rows;
+    const int w = BN / split;
+    const int col0 = rank * w;
+    const int g4 = max(0, min(w, min(BN, st.N - st.n0) - col0)) >> 2;   // float4 groups in the slice
+    const int items = vr * g4;
+    // C of the slice: every row prefetched into L2 now, the first pass loaded into registers,
+    // both while the tile accumulates
+    if (st.has_c && te < vr && g4 > 0)
+        prefetch_l2_bulk(st.c + (st.d_row + te) * st.N + st.n0 + col0, static_cast<uint32_t>(g4) * 16u);
+    float4 cv[kB];
+    long long gofs[kB];
+    uint32_t xofs[kB];
+    auto locate = [&](int u0) {
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            const int u = u0 + b * 128 + te;
+            const int rr = u < items ? u / g4 : 0;
+            const int cc = u < items ? col0 + 4 * (u - rr * g4) : 0;
+            gofs[b] = (st.d_row + rr) * st.N + st.n0 + cc;
+            xofs[b] = static_cast<uint32_t>(rr * C::kXStride + cc) * 4u;
+            cv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (u < items && st.has_c) cv[b] = *reinterpret_cast<const float4*>(st.c + gofs[b]);
+        }
+    };
+    locate(0);
+    const bool ok = wait_bar(accf, acc_ph, wctl, kWaitEpilogue);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    tc_fence_after();
+    fence_proxy_async_smem();   // the ring was last used by TMA and the tensor cores
+    if (q * 32 < vr) {
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t r[32];
+            if (st.nkb > 0) {
+                tmem_ld_32x32b_x32(tmem_acc + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = 0u;
+            }
+            if (row < vr) {
+                float4* dst = reinterpret_cast<float4*>(xb + row * C::kXStride + c0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive(acce);
+        for (int r2 = 0; r2 < split; ++r2) mbar_arrive_remote(map_shared_rank(xfull, r2));
+    }
+    const bool okx = wait_bar<true>(xfull, x_ph, wctl, kWaitExchange);
+    if (!__all_sync(0xffffffffu, okx)) return false;
+    const uint32_t xb_u32 = smem_u32(xb);
+    for (int u0 = 0; u0 < items; u0 += 128 * kB) {
+        if (u0 > 0) locate(u0);
+        float4 v[kB];
+        for (int r2 = 0; r2 < split; ++r2) {
+            const uint32_t base = map_shared_rank(xb_u32, r2);
+            float4 x[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b)
+                x[b] = (u0 + b * 128 + te < items) ? ld_dsmem_f32x4(base + xofs[b]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                if (r2 == 0) {
+                    v[b] = x[b];
+                } else {
+                    v[b].x += x[b].x; v[b].y += x[b].y; v[b].z += x[b].z; v[b].w += x[b].w;
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+            if (u0 + b * 128 + te >= items) continue;
+            const float4 o = make_float4(v[b].x + cv[b].x, v[b].y + cv[b].y, v[b].z + cv[b].z, v[b].w + cv[b].w);
+            if (st.d_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(st.d) + gofs[b]) = o;
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z, o.w);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(st.d) + gofs[b]) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            }
+        }
+    }
+    return true;
+}
+
+template <int BN, bool kTN, bool k2Sm, bool kSplit>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                const __grid_constant__ CUtensorMap tm_d) {
     static_assert(!(kTN && k2Sm), "CTA pairs are used by the NT kernels only");
+    static_assert(!(kSplit && (kTN || k2Sm)), "split-K clusters are a dense NT variant");
     using C = TileCfg<BN, k2Sm>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA pair: rank 0 (leader) issues the MMAs for both CTAs; rank 1 holds the other 128 rows.
-    const int rank = k2Sm ? static_cast<int>(cluster_ctarank()) : 0;
-    const bool leader = rank == 0;
+    // Split-K cluster: rank r runs the r-th share of the K-groups (every CTA is its own leader).
+    const int split = kSplit ? p.split : 1;   // a compile-time 1 outside the split-K variant
+    const int rank = (k2Sm || split > 1) ? static_cast<int>(cluster_ctarank()) : 0;
+    const bool leader = !k2Sm || rank == 0;
 
     const uint32_t bar0 = sbase + C::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -287,6 +429,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     auto cfull_bar = [&](int ew, int slot) {
         return bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + ew * C::kSlots + slot);
     };
+    const uint32_t xfull_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + 4 * C::kSlots);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     int* sched = reinterpret_cast<int*>(smem + C::kOffSched);
@@ -307,6 +450,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         }
         mbar_init(mma_drain_bar, 1);
         for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
+        mbar_init(xfull_bar, 4 * split);   // split-K: every epilogue warp of the cluster
         *abort_flag = 0;
         fence_mbar_init();
         if (p.K > 0) {          // a K-grouped call with K_total == 0 has no operand maps
@@ -316,6 +460,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         tma_prefetch_map(&tm_d);
         if (p.has_c) tma_prefetch_map(&tm_c);
     }
+    // Nothing above touched global memory (the tensor maps are kernel parameters): under a
+    // programmatic launch this is where the previous grid's results become visible.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) grid_launch_dependents();
     // Group tables for the masked (tile prefix) and K-grouped (K-group prefix) layouts.
     int total_tiles = p.num_mb * p.num_nb;
     if (warp == 2) {
@@ -367,12 +515,19 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         }
     }
     tc_fence_before();
-    if constexpr (k2Sm) cluster_sync();   // the pair's barriers are initialised before either CTA uses them
+    // the cluster's barriers are initialised before any CTA of it arrives on them remotely
+    if (k2Sm || split > 1) cluster_sync();
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (p.kind == kMasked) total_tiles = sched[p.G];
     if (p.kind == kKGrouped) total_tiles = sched[p.G] < 0 ? 0 : p.G * p.num_mb * p.num_nb;
+    if (split > 1 && (p.kind != kDense || static_cast<int>(cluster_nctarank()) != split ||
+                      static_cast<long long>(total_tiles) * split > gridDim.x)) {
+        // the exchange assumes one tile per cluster of `split` CTAs: refuse anything else
+        if (threadIdx.x == 0) record_status(p.status, kErrContract | kChkSplit);
+        total_tiles = 0;
+    }
 
     const WaitCtl wctl{abort_flag, p.status, p.timeout_ns};
 
@@ -384,7 +539,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             bool stall = p.debug_stall != 0 && leader;
             uint32_t armed = 0, armed_par = 0;   // per-stage: armed at least once / parity
             bool aborted = false;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
             Tile tl;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
                 for (int kb = 0; kb < tl.nkb; ++kb) {
@@ -403,7 +558,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                             tma_load_2d_pair(sa, &tm_a, fbl, kc, tl.a_coord);
                             tma_load_2d_pair(sb, &tm_b, fbl, kc, tl.b_coord);
                         } else if (!kTN) {
-                            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
+                            mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK + C::kBBytes);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
                             tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
                         } else {
@@ -433,7 +588,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             // completion (local barrier, 32 scale-loader lanes) to the leader's stage barrier.
             int s = 0;
             uint32_t ph = 0;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
             Tile tl;
             bool aborted = false;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
@@ -452,7 +607,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             uint32_t acc_ph = 0;
             uint32_t kcount = 0;
             bool aborted = false;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
             Tile tl;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
                 if (!wait_bar<k2Sm>(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
@@ -521,7 +676,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         // when they land, so this warp never waits for global-load latency.
         int s = 0;
         uint32_t ph = 0;
-        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile tl;
         bool aborted = false;
         while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
@@ -569,9 +724,9 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         const bool kg = p.kind == kKGrouped;
 
         // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
-        TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank);
+        TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile ctl;
-        bool c_have = p.has_c ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
+        bool c_have = (p.has_c && split == 1) ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
         int c_chunk = 0;
         uint32_t c_issued = 0;       // chunks whose C load has been issued
         auto issue_c = [&](uint32_t chunk_id) {
@@ -598,9 +753,23 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         uint32_t acc_ph = 0;
         uint32_t chunk_id = 0;       // chunks consumed so far
         bool aborted = false;
-        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank);
+        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile tl;
-        while (it.next(p, total_tiles, sched, cnt, tl)) {
+        if constexpr (kSplit) {
+            // split-K: one tile per cluster, exchanged through distributed shared memory
+            uint32_t x_ph = 0;
+            while (it.next(p, total_tiles, sched, cnt, tl)) {
+                const SplitTile st{tl.valid_rows, tl.n0, p.N, tl.nkb, tl.d_row, p.has_c, p.d_f32, p.c, p.d};
+                if (!split_k_tile<BN, C>(st, reinterpret_cast<float*>(smem + C::kOffA), tmem_base + acc * BN,
+                                         accf_bar(acc), acc_ph, acce_bar(acc), xfull_bar, x_ph, wctl, rank, split)) {
+                    aborted = true;
+                    break;
+                }
+                x_ph ^= 1u;
+                if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
+            }
+        }
+        while (split == 1 && it.next(p, total_tiles, sched, cnt, tl)) {
             // warp-uniform decision before the .sync.aligned TMEM loads below
             const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
             if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
@@ -746,14 +915,16 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             // C loads issued but never consumed (abort) must land before the CTA exits.
             for (uint32_t c = chunk_id; c < c_issued; ++c)
                 drain_bar(cfull_bar(ew, static_cast<int>(c % C::kSlots)), (c / C::kSlots) & 1u, 20000000ull);
-            bulk_wait_group<0>();
+            bulk_wait_group_read<0>();   // the slots are read; the stores complete with the grid
         }
         __syncwarp();
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    if constexpr (k2Sm) cluster_sync();   // the leader's MMAs may use this CTA's memory until here
+    // pair: the leader's MMAs may use this CTA's memory until here; split-K: peers read
+    // this CTA's exchange buffer until here
+    if (k2Sm || split > 1) cluster_sync();
     else __syncthreads();
     if (warp == 1) {
         tc_fence_after();

@@ -12,4 +12,7 @@ template cudaError_t launch_gemm<256, false>(const GemmParams&, const CUtensorMa
 template cudaError_t launch_gemm<128, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 template cudaError_t launch_gemm<224, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
 template cudaError_t launch_gemm<256, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t max_active_clusters<128, false, true>(int, int*);
+template cudaError_t max_active_clusters<224, false, true>(int, int*);
+template cudaError_t max_active_clusters<256, false, true>(int, int*);
 }  // namespace fg

@@ -1,0 +1,17 @@
+// fg_gemm_split.cu - split-K cluster variants of the dense NT kernel (one tile per
+// cluster, partial tiles summed through distributed shared memory), compiled in their
+// own translation unit.
+#include "fg_gemm_inst.cuh"
+
+namespace fg {
+template cudaError_t launch_gemm<64, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<128, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<192, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<224, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t max_active_clusters<64, false, false, true>(int, int*);
+template cudaError_t max_active_clusters<128, false, false, true>(int, int*);
+template cudaError_t max_active_clusters<192, false, false, true>(int, int*);
+template cudaError_t max_active_clusters<224, false, false, true>(int, int*);
+template cudaError_t max_active_clusters<256, false, false, true>(int, int*);
+}  // namespace fg

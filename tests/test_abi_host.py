@@ -46,6 +46,14 @@ def test_pure_host_utilities(fg):
     assert fg.lib.fg_status_string(-5).decode().startswith("bounded wait")
 
 
+def test_pdl_switch(fg):
+    assert fg.get_pdl() is True            # enabled by default
+    fg.set_pdl(False)
+    assert fg.get_pdl() is False
+    fg.set_pdl(True)
+    assert fg.get_pdl() is True
+
+
 FAKE = 1 << 20          # a 16-byte aligned non-null "device" address; never dereferenced
 
 

@@ -310,3 +310,116 @@ def test_scale_probe_cta_pairs(fg, monkeypatch):
     for gg in range(groups):
         want += 2.0 ** (7 + ea[:, gg][:, None] + eb[np.arange(n) // 128, gg][None, :])
     assert np.array_equal(out.values(), want)
+
+
+# ------------------------------------------------------------ split-K clusters
+def _launched_split(capfd):
+    err = capfd.readouterr().err
+    lines = [ln for ln in err.splitlines() if ln.startswith("[fg] fp8_gemm_nt")]
+    assert lines, err
+    return int(lines[-1].split("split=")[1].split()[0])
+
+
+@pytest.mark.parametrize("split", ["2", "4", "8"])
+@pytest.mark.parametrize("bn,out,with_c", [
+    ("64", "f32", True), ("128", "bf16", False), ("192", "f32", True), ("224", "bf16", False),
+    ("256", "f32", True),
+])
+@pytest.mark.parametrize("m,n,k", [
+    (100, 800, 1280),     # one ragged row block, N tail, 10 K-groups (uneven shares)
+    (40, 480, 640),       # <= 64 rows (64-row A box); 5 K-groups: with 8 CTAs some run none
+])
+def test_dense_split_k(fg, split, bn, out, with_c, m, n, k, monkeypatch, capfd):
+    """Split-K clusters: the CTAs of a cluster share one tile along K and sum their
+    partial tiles through distributed shared memory."""
+    monkeypatch.setenv("FG_FORCE_SPLIT", split)
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    case = C.dense_case(71 + m + int(bn) + int(split), m, n, k, with_c, out)
+    got = run_dense(fg, case)
+    assert _launched_split(capfd) == int(split)
+    C.compare(got.values(), C.dense_ref(case), f"split-K {split} BN={bn} {m}x{n}x{k}")
+
+
+def test_dense_split_k_aliased_c(fg, monkeypatch, capfd):
+    monkeypatch.setenv("FG_FORCE_SPLIT", "4")
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    case = C.dense_case(83, 64, 1024, 2048, True, "f32")
+    got = run_dense(fg, case, alias_c=True)
+    assert _launched_split(capfd) == 4
+    C.compare(got.values(), C.dense_ref(case), "split-K aliased C")
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+def test_scale_probe_split_k(fg, split, monkeypatch, capfd):
+    """The scale-identification probe under a K split: partial sums of distinct powers
+    of two stay exact, so the result is still bit-exact."""
+    from gpu_util import GuardedOut, dev
+    monkeypatch.setenv("FG_FORCE_SPLIT", split)
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    m, n, groups = 120, 512, 8
+    ea, eb = P.scale_probe_inputs(m, n, groups)
+    a = np.full((m, groups * 128), 0x38, np.uint8)
+    b = np.full((n, groups * 128), 0x38, np.uint8)
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_gemm_nt(dev(a), dev(F.pack_ue8m0((ea + 127).astype(np.uint8))), dev(b),
+                   dev(F.pack_ue8m0((eb + 127).astype(np.uint8))), out.tensor)
+    _status_ok(fg)
+    out.check_guards()
+    assert _launched_split(capfd) == int(split)
+    want = np.zeros((m, n))
+    for gg in range(groups):
+        want += 2.0 ** (7 + ea[:, gg][:, None] + eb[np.arange(n) // 128, gg][None, :])
+    assert np.array_equal(out.values(), want)
+
+
+# ------------------------------------------- programmatic dependent launch order
+def _gemm(fg, case, d, c=None):
+    from gpu_util import dev
+    fg.fp8_gemm_nt(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), d, c=c)
+
+
+def _chain(fg, pdl):
+    """Back-to-back GEMMs with no host synchronisation between them.
+    Read after write: a slow GEMM (K=4096) writes X, then a fast one (K=128) reads X as C.
+    Write after read: a slow GEMM reads X2 as C, then a fast one overwrites X2.
+    X and X2 start as NaN sentinels, so any premature read or write shows."""
+    from gpu_util import GuardedOut, dev
+    fg.set_pdl(pdl)
+    m, n = 512, 1024
+    slow = C.dense_case(91, m, n, 4096, False, "f32")
+    fast = C.dense_case(92, m, n, 128, True, "f32")
+    x, y = GuardedOut(m, n, "f32"), GuardedOut(m, n, "f32")
+    x2, y2 = GuardedOut(m, n, "f32"), GuardedOut(m, n, "f32")
+    x2.fill_from(fast["c"])
+    ops = [dev(t) for t in (slow["a"], slow["sfa"], slow["b"], slow["sfb"], fast["a"], fast["sfa"],
+                            fast["b"], fast["sfb"])]
+    torch.cuda.synchronize()
+    fg.fp8_gemm_nt(ops[0], ops[1], ops[2], ops[3], x.tensor)                  # X = slow
+    fg.fp8_gemm_nt(ops[4], ops[5], ops[6], ops[7], y.tensor, c=x.tensor)      # Y = X + fast
+    fg.fp8_gemm_nt(ops[0], ops[1], ops[2], ops[3], y2.tensor, c=x2.tensor)    # Y2 = X2 + slow
+    fg.fp8_gemm_nt(ops[4], ops[5], ops[6], ops[7], x2.tensor)                 # X2 = fast (no C)
+    _status_ok(fg)
+    for g in (x, y, x2, y2):
+        g.check_guards()
+    return slow, fast, x, y, x2, y2
+
+
+def test_pdl_dependent_launch_order(fg):
+    try:
+        slow, fast, x, y, x2, y2 = _chain(fg, True)
+        rows = np.array([0, 1, 127, 128, 300, 511])
+        slow_ref = C.dense_ref(slow, rows=rows)
+        fast_nc = dict(fast, c=None)
+        fast_ref = C.dense_ref(fast_nc, rows=rows)
+        C.compare(x.values()[rows], slow_ref, "X = slow")
+        C.compare(y.values()[rows], slow_ref + fast_ref, "Y = X + fast (read after write)")
+        C.compare(y2.values()[rows], fast["c"][rows] + slow_ref, "Y2 = X2 + slow (write after read)")
+        C.compare(x2.values()[rows], fast_ref, "X2 = fast")
+        # results never depend on the launch mode
+        bits_on = [g.inner_bits().copy() for g in (x, y, x2, y2)]
+        _, _, *outs_off = _chain(fg, False)
+        for a, g in zip(bits_on, outs_off):
+            assert np.array_equal(a, g.inner_bits())
+    finally:
+        fg.set_pdl(True)
