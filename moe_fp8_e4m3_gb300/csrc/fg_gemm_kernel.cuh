@@ -438,10 +438,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
     // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            // producer arrive (+ TMA bytes of both CTAs in pair mode), 32 scale-loader lanes,
-            // and in pair mode the peer's scale relay; the peer's own barrier counts only
-            // its scale-loader lanes.
-            mbar_init(full_bar(s), k2Sm ? (leader ? 34 : 32) : 33);
+            // One CTA: producer arrive (A bytes), scale-loader lane 0 arrive (B bytes), 32
+            // scale-loader lanes (cp.async).  Pair mode: producer arrive (TMA bytes of both
+            // CTAs), 32 scale-loader lanes and the peer's scale relay; the peer's own barrier
+            // counts only its scale-loader lanes.
+            mbar_init(full_bar(s), k2Sm ? (leader ? 34 : 32) : 34);
             mbar_init(empty_bar(s), 1);    // tcgen05.commit of the MMA issuer
         }
         for (int b = 0; b < C::kNumAcc; ++b) {
@@ -549,24 +550,20 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                     } else {
                         const uint32_t fb = full_bar(s);
                         const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
-                        const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
                         const int kc = (tl.kb0 + kb) * 128;
                         if constexpr (k2Sm) {
+                            const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
                             // both CTAs' tiles complete on the leader's barrier
                             if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kABytes + C::kBBytes));
                             const uint32_t fbl = map_shared_rank(fb, 0);
                             tma_load_2d_pair(sa, &tm_a, fbl, kc, tl.a_coord);
                             tma_load_2d_pair(sb, &tm_b, fbl, kc, tl.b_coord);
-                        } else if (!kTN) {
-                            mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK + C::kBBytes);
+                        } else if (!kTN) {   // B is loaded by the scale-loader warp
+                            mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
-                            tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
                         } else {
-                            mbar_arrive_expect_tx(fb, C::kABytes + C::kBBytes);
+                            mbar_arrive_expect_tx(fb, C::kABytes);
                             tma_load_2d(sa, &tm_a, fb, tl.a_coord, kc);
-#pragma unroll
-                            for (int h = 0; h < BN / 128; ++h)
-                                tma_load_2d(sb + h * 16384, &tm_b, fb, tl.b_coord + h * 128, kc);
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -674,8 +671,12 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
         // (lane, j) of each 32x4 atom holds MN index j * 32 + lane; rows outside the
         // problem are zero-filled).  Each lane's copies arrive on the stage's full barrier
         // when they land, so this warp never waits for global-load latency.
+        // One CTA: lane 0 also issues the stage's B tile.  A warp's TMA loads complete one
+        // after another (measured ~0.25-0.4 us each on GB300 whatever their size), so A and
+        // B from two warps stream in parallel.
         int s = 0;
         uint32_t ph = 0;
+        uint32_t armed = 0, armed_par = 0;   // stages whose B load this warp issued / parity
         TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile tl;
         bool aborted = false;
@@ -686,6 +687,24 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                 // warp-uniform decision: every lane leaves together on abort
                 const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
+                if constexpr (!k2Sm) {
+                    if (lane == 0) {
+                        const uint32_t fb = full_bar(s);
+                        const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
+                        const int kc = (tl.kb0 + kb) * 128;
+                        mbar_arrive_expect_tx(fb, C::kBBytes);
+                        if constexpr (!kTN) {
+                            tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < BN / 128; ++h)
+                                tma_load_2d(sb + h * 16384, &tm_b, fb, tl.b_coord + h * 128, kc);
+                        }
+                        armed |= 1u << s;
+                        armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    }
+                    __syncwarp();
+                }
                 const int kw = (tl.kb0 + kb) >> 2;
                 const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
                 const uint32_t da = sbase + C::kOffSfa + s * C::kSfaBytes + lane * 16;
@@ -711,6 +730,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
             }
         }
         cp_async_wait_all();
+        if (!k2Sm && lane == 0 && (aborted || *abort_flag)) {
+            // Bounded drain of B loads that may still be landing in shared memory.
+            for (int i = 0; i < C::kStages; ++i)
+                if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
+        }
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
