@@ -265,13 +265,12 @@ void fill_common(GemmParams& p, const DeviceState& st) {
     p.pdl = g_pdl;
 }
 
-int launch_nt_pair(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
-                   const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
+int launch_nt_pair(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
     switch (bn) {
-        case 128: e = fg::launch_gemm<128, false, true>(p, ma, mb, mc, md, grid, s); break;
-        case 224: e = fg::launch_gemm<224, false, true>(p, ma, mb, mc, md, grid, s); break;
-        default: e = fg::launch_gemm<256, false, true>(p, ma, mb, mc, md, grid, s); break;
+        case 128: e = fg::launch_gemm<128, false, true>(p, gm, grid, s); break;
+        case 224: e = fg::launch_gemm<224, false, true>(p, gm, grid, s); break;
+        default: e = fg::launch_gemm<256, false, true>(p, gm, grid, s); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -286,16 +285,15 @@ int use_pair_mode() {
     return e && e[0] == '1';
 }
 
-int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
-              const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
+int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
     if (p.split > 1) {
         switch (bn) {
-            case 64: e = fg::launch_gemm<64, false, false, true>(p, ma, mb, mc, md, grid, s); break;
-            case 128: e = fg::launch_gemm<128, false, false, true>(p, ma, mb, mc, md, grid, s); break;
-            case 192: e = fg::launch_gemm<192, false, false, true>(p, ma, mb, mc, md, grid, s); break;
-            case 224: e = fg::launch_gemm<224, false, false, true>(p, ma, mb, mc, md, grid, s); break;
-            default: e = fg::launch_gemm<256, false, false, true>(p, ma, mb, mc, md, grid, s); break;
+            case 64: e = fg::launch_gemm<64, false, false, true>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, false, false, true>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, false, false, true>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, false, false, true>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, false, false, true>(p, gm, grid, s); break;
         }
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -304,11 +302,11 @@ int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensor
         return FG_OK;
     }
     switch (bn) {
-        case 64: e = fg::launch_gemm<64, false>(p, ma, mb, mc, md, grid, s); break;
-        case 128: e = fg::launch_gemm<128, false>(p, ma, mb, mc, md, grid, s); break;
-        case 192: e = fg::launch_gemm<192, false>(p, ma, mb, mc, md, grid, s); break;
-        case 224: e = fg::launch_gemm<224, false>(p, ma, mb, mc, md, grid, s); break;
-        default: e = fg::launch_gemm<256, false>(p, ma, mb, mc, md, grid, s); break;
+        case 64: e = fg::launch_gemm<64, false>(p, gm, grid, s); break;
+        case 128: e = fg::launch_gemm<128, false>(p, gm, grid, s); break;
+        case 192: e = fg::launch_gemm<192, false>(p, gm, grid, s); break;
+        case 224: e = fg::launch_gemm<224, false>(p, gm, grid, s); break;
+        default: e = fg::launch_gemm<256, false>(p, gm, grid, s); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -317,10 +315,9 @@ int launch_nt(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensor
     return FG_OK;
 }
 
-int launch_tn(int bn, const GemmParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
-              const CUtensorMap& mc, const CUtensorMap& md, int grid, cudaStream_t s) {
-    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, ma, mb, mc, md, grid, s)
-                                    : fg::launch_gemm<256, true>(p, ma, mb, mc, md, grid, s);
+int launch_tn(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, gm, grid, s)
+                                    : fg::launch_gemm<256, true>(p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -380,7 +377,9 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     // a single row block of at most 64 rows: load only those rows of A (the MMA still
     // reads 128 rows of shared memory; rows past M produce accumulator rows never stored)
     p.a_box_rows = (!pair && M <= 64) ? 64 : 128;
-    CUtensorMap ma, mb, mc, md;
+    fg::GemmMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, pair ? bn / 2 : bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -402,8 +401,8 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     if (print_configs())
         std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d%s\n", M, N, K, bn,
                      p.split, tiles, grid, pair ? " (CTA pairs)" : "");
-    if (pair) return launch_nt_pair(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
-    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (pair) return launch_nt_pair(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
@@ -433,7 +432,9 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     p.m_indices = m_indices;
     p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb, mc, md;
+    fg::GemmMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -444,7 +445,7 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
                      M_total, N, K, G, bn, grid);
-    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
@@ -474,7 +475,9 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     p.masked_m = masked_m;
     p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb, mc, md;
+    fg::GemmMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -484,7 +487,7 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_masked G=%d M_max=%d N=%d K=%d BN=%d grid=%d\n", G, M_max, N, K, bn, grid);
-    return launch_nt(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const uint8_t* a,
@@ -516,7 +519,9 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     p.ks = ks;
     p.d = d;
     fill_common(p, *st);
-    CUtensorMap ma, mb, mc, md;
+    fg::GemmMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
     std::memset(&ma, 0, sizeof(ma));
     std::memset(&mb, 0, sizeof(mb));
     std::memset(&mc, 0, sizeof(mc));
@@ -526,6 +531,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
         (c && !encode_3d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M, G, pitch1, pitch2, 32, 32,
                          CU_TENSOR_MAP_SWIZZLE_128B)))
         return FG_ERR_INVALID_ARG;
+
     // With K_total == 0 every segment is empty and no operand load is ever issued.
     if (K_total > 0 &&
         (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K_total, M, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -535,7 +541,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] k_grouped_tn G=%d M=%d N=%d K_total=%d BN=%d grid=%d\n", G, M, N, K_total, bn, grid);
-    return launch_tn(bn, p, ma, mb, mc, md, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_tn(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_get_mk_alignment_for_contiguous_layout(void) { return 128; }

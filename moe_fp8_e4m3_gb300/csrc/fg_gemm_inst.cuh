@@ -48,8 +48,7 @@ inline void set_launch_attrs(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr,
 }
 
 template <int BN, bool kTN, bool k2Sm, bool kSplit>
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream) {
     cudaError_t err = configure_gemm<BN, kTN, k2Sm, kSplit>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
@@ -59,7 +58,7 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUt
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, k2Sm ? 2 : (kSplit ? p.split : 1), p.pdl != 0);
-    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kTN, k2Sm, kSplit>, p, map_a, map_b, map_c, map_d);
+    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kTN, k2Sm, kSplit>, p, maps);
 }
 
 template <int BN, bool kTN, bool k2Sm, bool kSplit>

@@ -64,6 +64,12 @@ enum : int {
 constexpr int kMaxGroups = 256;   // masked / K-grouped groups held in shared memory
 constexpr int kSmemLimit = 232448;
 
+// Tensor maps of one launch (a kernel parameter, so the TMA unit reads them from
+// parameter space): A and B operand tiles, C and D 32-row x 128-byte epilogue boxes.
+struct GemmMaps {
+    CUtensorMap a, b, c, d;
+};
+
 struct GemmParams {
     int kind;
     int M, N, K;           // dense M,N,K | contiguous M_total | masked M_max | K-grouped M,N,K_total
@@ -404,9 +410,11 @@ __device__ __noinline__ bool split_k_tile(const SplitTile st, float* xb, uint32_
 
 template <int BN, bool kTN, bool k2Sm, bool kSplit>
 __global__ void __launch_bounds__(224, 1)
-fg_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tm_a,
-               const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
-               const __grid_constant__ CUtensorMap tm_d) {
+fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
+    const CUtensorMap& tm_a = maps.a;
+    const CUtensorMap& tm_b = maps.b;
+    const CUtensorMap& tm_c = maps.c;
+    const CUtensorMap& tm_d = maps.d;
     static_assert(!(kTN && k2Sm), "CTA pairs are used by the NT kernels only");
     static_assert(!(kSplit && (kTN || k2Sm)), "split-K clusters are a dense NT variant");
     using C = TileCfg<BN, k2Sm>;

@@ -4,11 +4,11 @@
 #include "fg_gemm_inst.cuh"
 
 namespace fg {
-template cudaError_t launch_gemm<64, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<128, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<192, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<224, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
-template cudaError_t launch_gemm<256, false, false, true>(const GemmParams&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t);
+template cudaError_t launch_gemm<64, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<128, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<192, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<224, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
 template cudaError_t max_active_clusters<64, false, false, true>(int, int*);
 template cudaError_t max_active_clusters<128, false, false, true>(int, int*);
 template cudaError_t max_active_clusters<192, false, false, true>(int, int*);

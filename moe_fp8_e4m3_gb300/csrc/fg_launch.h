@@ -13,8 +13,7 @@ namespace fg {
 // k2Sm: clusters of two CTAs sharing one 256-row MMA (dense NT only).
 // kSplit: clusters of p.split CTAs sharing one tile along K (dense NT only).
 template <int BN, bool kTN, bool k2Sm = false, bool kSplit = false>
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_c, const CUtensorMap& map_d, int grid, cudaStream_t stream);
+cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream);
 
 // How many clusters of `cluster` CTAs of fg_gemm_kernel<BN, kTN, k2Sm, kSplit> can be resident at once.
 template <int BN, bool kTN, bool k2Sm = false, bool kSplit = false>
