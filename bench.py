@@ -17,7 +17,8 @@ Two timed passes of --steps steps each:
   2. the per-kernel durations (the roofline and the per-kernel breakdown): an event
      between consecutive GEMMs, which serialises them.
 
-Other workloads (--workload prefill | decode | contiguous | masked | k_grouped) time the
+Other workloads (--workload prefill | decode | contiguous | masked | k_grouped, and the
+other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn) time the
 single GEMMs on the same rules; they are measurement aids, the default line is the headline.
 
 Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
@@ -43,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_split.cu",
-                  "fg_gemm_tn.cu"]
+                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu"]
 
 
 def align4(x: int) -> int:
@@ -382,7 +383,57 @@ class Decode(DensePair):
     SHAPES = [("decode", 64, 7168, 4096)]
 
 
-WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped)}
+class _PrefillLayout(Prefill):
+    """The prefill GEMM with its operands stored in another layout (same values, same
+    bytes and FLOPs): A as [K, M] for a leading T, B as [K, N] for a trailing N."""
+    LAYOUT = "nn"
+
+    def __init__(self, torch, fg, seed):
+        super().__init__(torch, fg, seed)
+        p = self.parts[0]
+        if self.LAYOUT[0] == "t":
+            p["a"] = p["a"].t().contiguous()
+        if self.LAYOUT[1] == "n":
+            p["b"] = p["b"].t().contiguous()
+        torch.cuda.synchronize()
+
+    def launches(self):
+        fn = getattr(self.fg, "fp8_gemm_" + self.LAYOUT)
+        return [lambda p=p: fn(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], c=p["c"]) for p in self.parts]
+
+
+class PrefillNN(_PrefillLayout):
+    name, LAYOUT = "prefill_nn", "nn"
+    description = "dense FP8 NN GEMM (B stored [K,N]) M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
+
+
+class PrefillTN(_PrefillLayout):
+    name, LAYOUT = "prefill_tn", "tn"
+    description = "dense FP8 TN GEMM (A [K,M], B [K,N]) M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
+
+
+class PrefillTT(_PrefillLayout):
+    name, LAYOUT = "prefill_tt", "tt"
+    description = "dense FP8 TT GEMM (A stored [K,M]) M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
+
+
+class ContiguousNN(Contiguous):
+    """The contiguous workload with each expert's weights stored [K, N]."""
+    name = "contiguous_nn"
+    description = Contiguous.description.replace("contiguous FP8 NT GEMM", "contiguous FP8 NN GEMM (B [G,K,N])")
+
+    def __init__(self, torch, fg, seed):
+        super().__init__(torch, fg, seed)
+        self.b = self.b.transpose(1, 2).contiguous()
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_gemm_nn_contiguous(self.a, self.sfa, self.b, self.sfb,
+                                                                 self.m_indices, self.d)]
+
+
+WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped, PrefillNN, PrefillTN,
+                                 PrefillTT, ContiguousNN)}
 
 
 # ------------------------------------------------------------------- CPU oracle arm

@@ -40,7 +40,8 @@
  *     mask out of range, bad K segments) and internal wait time-outs never trap: the
  *     kernel skips the offending tile (or the whole call), records the first such
  *     event in a per-device status word and returns; fg_get_device_error reads it.
- *   - Results are deterministic: no atomics touch D, no split-K.
+ *   - Results are deterministic: no atomics touch D; when a dense GEMM with few tiles
+ *     is split along K, the partial tiles are summed in a fixed order.
  */
 #ifndef FG_H
 #define FG_H
@@ -82,6 +83,32 @@ int fg_fp8_gemm_nt(int M, int N, int K,
                    const float* c, void* d, int d_dtype, fg_stream_t stream);
 
 /*
+ * The other dense layouts (docsearch section 4 "Memory Layouts": SM100 supports NT, TN,
+ * NN and TT; section 9 item 1, fp8_gemm_{nt, nn, tn, tt}).  The same product
+ *   D[m,n] = C[m,n] + sum_k A(m,k) * B(k,n) with the same scales and C/D as the NT GEMM,
+ * with the operands stored as
+ *   NN:  a [M][K] (K contiguous),  b [K][N] (N contiguous)
+ *   TN:  a [K][M] (M contiguous),  b [K][N] (N contiguous)
+ *   TT:  a [K][M] (M contiguous),  b [N][K] (K contiguous)
+ * The letter says whether the operand is stored transposed relative to the NT form's
+ * A [M][K] and B^T = [N][K].  sfa and sfb keep the NT layouts (one scale per row of A
+ * and 1x128 K-group; one per 128x128 block of B) whatever the operand layout.
+ * Shapes as for fg_fp8_gemm_nt, plus M % 16 == 0 when A is stored [K][M] (TN, TT).
+ */
+int fg_fp8_gemm_nn(int M, int N, int K,
+                   const uint8_t* a, const int32_t* sfa,
+                   const uint8_t* b, const int32_t* sfb,
+                   const float* c, void* d, int d_dtype, fg_stream_t stream);
+int fg_fp8_gemm_tn(int M, int N, int K,
+                   const uint8_t* a, const int32_t* sfa,
+                   const uint8_t* b, const int32_t* sfb,
+                   const float* c, void* d, int d_dtype, fg_stream_t stream);
+int fg_fp8_gemm_tt(int M, int N, int K,
+                   const uint8_t* a, const int32_t* sfa,
+                   const uint8_t* b, const int32_t* sfb,
+                   const float* c, void* d, int d_dtype, fg_stream_t stream);
+
+/*
  * M-grouped contiguous NT GEMM (docsearch section 9 item 2; README "Grouped GEMMs
  * (contiguous layout)"): the token rows of all groups (experts) are concatenated
  * along M, every group segment aligned to fg_get_mk_alignment_for_contiguous_layout()
@@ -98,6 +125,19 @@ int fg_fp8_gemm_nt(int M, int N, int K,
  * M_total % 128 == 0, G >= 1.  No C operand.
  */
 int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G,
+                                        const uint8_t* a, const int32_t* sfa,
+                                        const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* m_indices,
+                                        void* d, int d_dtype, fg_stream_t stream);
+
+/*
+ * The same M-grouped contiguous GEMM with each group's weights stored N-major
+ * (docsearch section 9 item 2, m_grouped_fp8_gemm_{nt, nn}_contiguous):
+ *   D[m,:] = A[m,:] @ B[m_indices[m]],  b [G][K][N] E4M3 (N contiguous)
+ * Everything else (sfa, sfb, m_indices, d, padding rows, contract checks) as for
+ * fg_m_grouped_fp8_gemm_nt_contiguous.
+ */
+int fg_m_grouped_fp8_gemm_nn_contiguous(int M_total, int N, int K, int G,
                                         const uint8_t* a, const int32_t* sfa,
                                         const uint8_t* b, const int32_t* sfb,
                                         const int32_t* m_indices,

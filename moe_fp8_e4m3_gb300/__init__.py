@@ -27,7 +27,11 @@ _I = ctypes.c_int
 
 _SIGNATURES = {
     "fg_fp8_gemm_nt": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_fp8_gemm_nn": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_fp8_gemm_tn": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_fp8_gemm_tt": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_gemm_nt_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_m_grouped_fp8_gemm_nn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
     "fg_k_grouped_fp8_gemm_tn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_quantize_1x128_rows": (_I, [_I, _I, _P, _P, _P, _P]),
@@ -117,6 +121,41 @@ def fp8_gemm_nt(a, sfa, b, sfb, d, c=None, stream=None) -> None:
     n = b.shape[0]
     _check(lib.fg_fp8_gemm_nt(m, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                               code, _stream(stream)), "fp8_gemm_nt")
+
+
+def _dense_layout(fn, name, a, sfa, b, sfb, d, c, stream, a_t, b_n):
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _c(c)
+    code = _out(d, "d")
+    k, m = a.shape if a_t else a.shape[::-1]
+    n = b.shape[1] if b_n else b.shape[0]
+    _check(fn(m, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), code, _stream(stream)), name)
+
+
+def fp8_gemm_nn(a, sfa, b, sfb, d, c=None, stream=None) -> None:
+    """D = C + A @ B.  a [M,K], b [K,N] E4M3 (N contiguous); scales, c and d as fp8_gemm_nt."""
+    _dense_layout(lib.fg_fp8_gemm_nn, "fp8_gemm_nn", a, sfa, b, sfb, d, c, stream, False, True)
+
+
+def fp8_gemm_tn(a, sfa, b, sfb, d, c=None, stream=None) -> None:
+    """D = C + A.T @ B.  a [K,M] (M contiguous, M % 16 == 0), b [K,N]; scales, c and d as fp8_gemm_nt."""
+    _dense_layout(lib.fg_fp8_gemm_tn, "fp8_gemm_tn", a, sfa, b, sfb, d, c, stream, True, True)
+
+
+def fp8_gemm_tt(a, sfa, b, sfb, d, c=None, stream=None) -> None:
+    """D = C + A.T @ B.T.  a [K,M] (M contiguous, M % 16 == 0), b [N,K]; scales, c and d as fp8_gemm_nt."""
+    _dense_layout(lib.fg_fp8_gemm_tt, "fp8_gemm_tt", a, sfa, b, sfb, d, c, stream, True, False)
+
+
+def m_grouped_fp8_gemm_nn_contiguous(a, sfa, b, sfb, m_indices, d, stream=None) -> None:
+    """D[m] = A[m] @ B[m_indices[m]] for rows with m_indices[m] >= 0.  a [M_total,K];
+    b [G,K,N] (N contiguous); sfb [G, ceil(K/512), align4(ceil(N/128))]; m_indices int32 [M_total]."""
+    _fp8(a, "a"); _fp8(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _i32(m_indices, "m_indices")
+    code = _out(d, "d")
+    m_total, k = a.shape
+    g, _, n = b.shape
+    _check(lib.fg_m_grouped_fp8_gemm_nn_contiguous(m_total, n, k, g, _ptr(a), _ptr(sfa), _ptr(b),
+                                                   _ptr(sfb), _ptr(m_indices), _ptr(d), code,
+                                                   _stream(stream)), "m_grouped_fp8_gemm_nn_contiguous")
 
 
 def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, d, stream=None) -> None:

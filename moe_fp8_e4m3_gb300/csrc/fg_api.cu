@@ -315,9 +315,17 @@ int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cud
     return FG_OK;
 }
 
-int launch_tn(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
-    const cudaError_t e = bn == 128 ? fg::launch_gemm<128, true>(p, gm, grid, s)
-                                    : fg::launch_gemm<256, true>(p, gm, grid, s);
+// Variants with an MN-major operand (kMajTN, kMajNN, kMajTT): BN 128 or 256, and 224 for TT.
+int launch_mn(int maj, int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    cudaError_t e;
+    if (maj == fg::kMajTN)
+        e = bn == 128 ? fg::launch_gemm<128, fg::kMajTN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajTN>(p, gm, grid, s);
+    else if (maj == fg::kMajNN)
+        e = bn == 128 ? fg::launch_gemm<128, fg::kMajNN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajNN>(p, gm, grid, s);
+    else if (bn == 224)
+        e = fg::launch_gemm<224, fg::kMajTT>(p, gm, grid, s);
+    else
+        e = bn == 128 ? fg::launch_gemm<128, fg::kMajTT>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajTT>(p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -405,10 +413,14 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
-                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
-                                        const int32_t* m_indices, void* d, int d_dtype,
-                                        fg_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// M-grouped contiguous GEMM; b_nmajor: B stored [G][K][N] (NN) instead of [G][N][K] (NT).
+int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const uint8_t* a, const int32_t* sfa,
+                         const uint8_t* b, const int32_t* sfb, const int32_t* m_indices, void* d, int d_dtype,
+                         fg_stream_t stream) {
     if (M_total < 0 || M_total % 128 != 0 || G < 1) return FG_ERR_INVALID_ARG;
     int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
     if (rc) return rc;
@@ -419,7 +431,7 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = M_total / 128;
-    const int bn = choose_bn_nt(num_mb, N, sms, false);
+    const int bn = b_nmajor ? choose_bn_tn(num_mb, N, sms, false) : choose_bn_nt(num_mb, N, sms, false);
     GemmParams p{};
     p.kind = fg::kContiguous;
     p.M = M_total; p.N = N; p.K = K; p.G = G;
@@ -432,20 +444,111 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
     p.m_indices = m_indices;
     p.d = d;
     fill_common(p, *st);
+    p.b_gstride_k = K;
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
-    std::memset(&mc, 0, sizeof(mc));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &md = gm.d;
+    const bool b_ok = b_nmajor
+        ? encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, (uint64_t)G * K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+        : encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_out_2d(&md, d, N, M_total, p.d_f32))
+        !b_ok || !encode_out_2d(&md, d, N, M_total, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
-        std::fprintf(stderr, "[fg] m_grouped_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
-                     M_total, N, K, G, bn, grid);
+        std::fprintf(stderr, "[fg] m_grouped_%s_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
+                     b_nmajor ? "nn" : "nt", M_total, N, K, G, bn, grid);
+    if (b_nmajor) return launch_mn(fg::kMajNN, bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Dense GEMM with an MN-major operand: maj = kMajNN (B [K][N]), kMajTN (A [K][M], B [K][N])
+// or kMajTT (A [K][M]).  Same scales, C and D as the NT GEMM.
+int dense_mn(int maj, int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+             const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    const bool a_mn = (maj & 1) != 0, b_mn = (maj & 2) != 0;
+    if (M < 0) return FG_ERR_INVALID_ARG;
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    if (rc) return rc;
+    if (a_mn && M % 16 != 0) return FG_ERR_INVALID_ARG;   // [K][M] rows: 16-byte TMA pitch
+    if (c && !aligned16(c)) return FG_ERR_INVALID_ARG;
+    if (c && d_dtype != FG_F32) return FG_ERR_UNSUPPORTED;
+    if (M == 0) return FG_OK;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    const int num_mb = ceil_div(M, 128);
+    int bn;
+    if (b_mn) {
+        bn = choose_bn_tn(num_mb, N, sms, c != nullptr);       // whole 128-column atoms of B
+    } else {                                                  // K-major B: the NT widths 128/224/256
+        const int b0 = choose_bn_nt(num_mb, N, sms, c != nullptr);
+        bn = b0 <= 128 ? 128 : (b0 <= 224 ? 224 : 256);
+    }
+    GemmParams p{};
+    fill_common(p, *st);
+    p.kind = fg::kDense;
+    p.M = M; p.N = N; p.K = K; p.G = 1;
+    p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
+    p.num_mb = num_mb;
+    p.num_nb = ceil_div(N, bn);
+    p.sfa = sfa; p.sfb = sfb;
+    p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_rows = M;
+    p.d = d;
+    p.c = c;
+    p.a_box_rows = (!a_mn && M <= 64) ? 64 : 128;
+    fg::GemmMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
+    const bool a_ok = a_mn
+        ? encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K, M, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+        : encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool b_ok = b_mn
+        ? encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+        : encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!a_ok || !b_ok || !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
+        return FG_ERR_INVALID_ARG;
+    const long long tiles = (long long)p.num_mb * p.num_nb;
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (print_configs())
+        std::fprintf(stderr, "[fg] fp8_gemm_%s M=%d N=%d K=%d BN=%d tiles=%lld grid=%d\n",
+                     maj == fg::kMajNN ? "nn" : (maj == fg::kMajTN ? "tn" : "tt"), M, N, K, bn, tiles, grid);
+    return launch_mn(maj, bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
+                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* m_indices, void* d, int d_dtype,
+                                        fg_stream_t stream) {
+    return m_grouped_contiguous(false, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
+}
+
+int fg_m_grouped_fp8_gemm_nn_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
+                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* m_indices, void* d, int d_dtype,
+                                        fg_stream_t stream) {
+    return m_grouped_contiguous(true, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
+}
+
+int fg_fp8_gemm_nn(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    return dense_mn(fg::kMajNN, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
+}
+
+int fg_fp8_gemm_tn(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    return dense_mn(fg::kMajTN, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
+}
+
+int fg_fp8_gemm_tt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    return dense_mn(fg::kMajTT, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
 }
 
 int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
@@ -515,6 +618,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(N);
+    p.sfb_per_row = 1;
     p.sfa_rows = M;
     p.ks = ks;
     p.d = d;
@@ -541,7 +645,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] k_grouped_tn G=%d M=%d N=%d K_total=%d BN=%d grid=%d\n", G, M, N, K_total, bn, grid);
-    return launch_tn(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+    return launch_mn(fg::kMajTN, bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fg_get_mk_alignment_for_contiguous_layout(void) { return 128; }

@@ -48,6 +48,11 @@ namespace fg {
 
 enum GemmKind : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 
+// Operand majors of a kernel variant (the pages' layout letters, D = C + A @ B):
+// bit 0 set = A stored [K][M] (M-major, "T"), clear = [M][K] (K-major, "N");
+// bit 1 set = B stored [K][N] (N-major, "N"), clear = [N][K] (K-major, "T").
+enum : int { kMajNT = 0, kMajTT = 1, kMajNN = 2, kMajTN = 3 };
+
 // Device status codes (the word keeps the first event).
 enum : int {
     kErrContract = 0x100,      // | check id
@@ -89,6 +94,8 @@ struct GemmParams {
     int split;             // CTAs per cluster sharing one tile along K (1: no split)
     int a_box_rows;        // rows of the A tensor-map box (128, or 64 when every tile has <= 64 rows)
     int pdl;               // host side: launch with programmatic stream serialisation
+    int sfb_per_row;       // B scales: one per row of B and 1x128 K-group (else one per 128x128 block)
+    long long b_gstride_k; // MN-major grouped B: rows of the [G*K][N] map between groups (K)
     int* status;
     unsigned long long timeout_ns;
     int debug_stall;
@@ -142,6 +149,7 @@ struct Tile {
     int g, n0;
     int a_coord, b_coord;   // NT: rows in the A/B maps; TN: columns (m0 / n0)
     int kb0, nkb;           // first global K-group and number of K-groups
+    long long b_krow;       // MN-major B: map row of the tile's K = 0 (group offset)
     int valid_rows;         // rows [0, valid_rows) of the tile lie inside the problem
     long long d_row;        // row of D (flat [rows][N] view) that holds the tile's row 0
     int d_y, d_z;           // coordinates of row 0 in the C/D tensor maps
@@ -200,6 +208,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
     tl.nkb = p.K / 128;
     tl.sfa_g = 0;
     tl.d_z = 0;
+    tl.b_krow = 0;
     if (p.kind == kDense) {
         const int mbq = t % p.num_mb, nb = t / p.num_mb;
         const int mb = pair ? 2 * mbq + rank : mbq;
@@ -225,6 +234,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
         tl.g = (g < 0 || g >= p.G) ? 0 : g;
         tl.a_coord = mb * 128;
         tl.b_coord = tl.g * p.N + tl.n0;
+        tl.b_krow = tl.g * p.b_gstride_k;
         tl.valid_rows = 128;
         tl.d_row = (long long)mb * 128;
         tl.sfa_row = mb * 128;
@@ -408,15 +418,17 @@ __device__ __noinline__ bool split_k_tile(const SplitTile st, float* xb, uint32_
     return true;
 }
 
-template <int BN, bool kTN, bool k2Sm, bool kSplit>
+template <int BN, int kMaj, bool k2Sm, bool kSplit>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_a = maps.a;
     const CUtensorMap& tm_b = maps.b;
     const CUtensorMap& tm_c = maps.c;
     const CUtensorMap& tm_d = maps.d;
-    static_assert(!(kTN && k2Sm), "CTA pairs are used by the NT kernels only");
-    static_assert(!(kSplit && (kTN || k2Sm)), "split-K clusters are a dense NT variant");
+    constexpr bool kAmn = (kMaj & 1) != 0, kBmn = (kMaj & 2) != 0;
+    static_assert(!(kMaj != kMajNT && k2Sm), "CTA pairs are used by the NT kernels only");
+    static_assert(!(kSplit && (kMaj != kMajNT || k2Sm)), "split-K clusters are a dense NT variant");
+    static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
     using C = TileCfg<BN, k2Sm>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -566,10 +578,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                             const uint32_t fbl = map_shared_rank(fb, 0);
                             tma_load_2d_pair(sa, &tm_a, fbl, kc, tl.a_coord);
                             tma_load_2d_pair(sb, &tm_b, fbl, kc, tl.b_coord);
-                        } else if (!kTN) {   // B is loaded by the scale-loader warp
+                        } else if (!kAmn) {   // B is loaded by the scale-loader warp
                             mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
-                        } else {
+                        } else {              // A [K][M]: one 128 (M) x 128 (K) box
                             mbar_arrive_expect_tx(fb, C::kABytes);
                             tma_load_2d(sa, &tm_a, fb, tl.a_coord, kc);
                         }
@@ -605,7 +617,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 }
             }
         } else if (lane == 0) {
-            constexpr uint32_t kIdesc = make_idesc_mxf8(k2Sm ? 256 : 128, BN, kTN, kTN);
+            constexpr uint32_t kIdesc = make_idesc_mxf8(k2Sm ? 256 : 128, BN, kAmn, kBmn);
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
@@ -642,13 +654,12 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint64_t ad, bd;
-                        if (!kTN) {   // K-major, 128-byte rows, 8-row swizzle atoms 1024 B apart
-                            ad = make_sdesc(sa + 32 * j, 0, 1024, kLayoutSw128);
-                            bd = make_sdesc(sb + 32 * j, 0, 1024, kLayoutSw128);
-                        } else {      // MN-major: 128-byte MN atoms 16 KB apart, 8 K rows per 1024 B
-                            ad = make_sdesc(sa + 4096 * j, 16384, 1024, kLayoutSw128);
-                            bd = make_sdesc(sb + 4096 * j, 16384, 1024, kLayoutSw128);
-                        }
+                        // K-major: 128-byte rows, 8-row swizzle atoms 1024 B apart, +32 B per K step;
+                        // MN-major: 128-byte MN atoms 16 KB apart, 8 K rows per 1024 B, +4 KB per K step
+                        ad = kAmn ? make_sdesc(sa + 4096 * j, 16384, 1024, kLayoutSw128)
+                                  : make_sdesc(sa + 32 * j, 0, 1024, kLayoutSw128);
+                        bd = kBmn ? make_sdesc(sb + 4096 * j, 16384, 1024, kLayoutSw128)
+                                  : make_sdesc(sb + 32 * j, 0, 1024, kLayoutSw128);
                         if constexpr (k2Sm) tc_mma_mxf8_pair(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
                         else tc_mma_mxf8(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
                     }
@@ -701,12 +712,13 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
                         const int kc = (tl.kb0 + kb) * 128;
                         mbar_arrive_expect_tx(fb, C::kBBytes);
-                        if constexpr (!kTN) {
+                        if constexpr (!kBmn) {
                             tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
-                        } else {
+                        } else {   // B [K][N] (grouped: [G*K][N]): 128 (N) x 128 (K) boxes
+                            const int krow = static_cast<int>(tl.b_krow) + kc;
 #pragma unroll
                             for (int h = 0; h < BN / 128; ++h)
-                                tma_load_2d(sb + h * 16384, &tm_b, fb, tl.b_coord + h * 128, kc);
+                                tma_load_2d(sb + h * 16384, &tm_b, fb, tl.n0 + h * 128, krow);
                         }
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -730,7 +742,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     for (int j = 0; j < 4; ++j) {
                         const int n = tl.n0 + i * 128 + j * 32 + lane;
                         const bool in = n < p.N;
-                        cp_async_4(db + i * 512 + 4 * j, in ? pb + (kTN ? n : (n >> 7)) : pb, in ? 4u : 0u);
+                        cp_async_4(db + i * 512 + 4 * j, in ? pb + (p.sfb_per_row ? n : (n >> 7)) : pb, in ? 4u : 0u);
                     }
                 }
                 cp_async_mbar_arrive(full_bar(s));

@@ -2,6 +2,6 @@
 #include "fg_gemm_inst.cuh"
 
 namespace fg {
-template cudaError_t launch_gemm<128, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
-template cudaError_t launch_gemm<256, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<128, kMajTN>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, kMajTN>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
 }  // namespace fg

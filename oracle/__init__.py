@@ -15,6 +15,6 @@ from . import formats, gemm  # noqa: F401
 from .formats import (e4m3_to_f64, f64_to_bf16, f64_to_e4m3, pack_ue8m0,  # noqa: F401
                       quantize_blocks, quantize_cols, quantize_rows, ue8m0_for_amax,
                       ue8m0_to_f64, unpack_ue8m0, bf16_to_f64, tma_aligned_size)
-from .gemm import (fp8_gemm_nt, k_grouped_fp8_gemm_tn_contiguous,  # noqa: F401
-                   m_grouped_fp8_gemm_nt_contiguous, m_grouped_fp8_gemm_nt_masked,
-                   round_output)
+from .gemm import (fp8_gemm_nn, fp8_gemm_nt, fp8_gemm_tn, fp8_gemm_tt,  # noqa: F401
+                   k_grouped_fp8_gemm_tn_contiguous, m_grouped_fp8_gemm_nn_contiguous,
+                   m_grouped_fp8_gemm_nt_contiguous, m_grouped_fp8_gemm_nt_masked, round_output)

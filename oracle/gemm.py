@@ -28,6 +28,13 @@ README "Grouped GEMMs (contiguous layout)" and "Grouped GEMMs (masked layout)"):
   [off_g, off_g + ks[g]) of A[K_total, M] and B[K_total, N];
   D[g] = C[g] + A_g.T @ B_g.
 
+The other dense layouts (docsearch section 4 "Memory Layouts"; section 9 item 1,
+``fp8_gemm_{nt, nn, tn, tt}``, and item 2, ``m_grouped_fp8_gemm_{nt, nn}_contiguous``)
+compute the same product with the operands stored differently: the first letter says
+whether A is stored as [M, K] (N) or [K, M] (T), the second whether B is stored
+transposed, [N, K] (T), or as [K, N] (N).  The scales keep their layouts.  Their oracle
+is the NT definition applied to the operands read in that storage order.
+
 Readings (also listed in the design doc): A scales are 1x128 per row; B scales are one
 per 128x128 block (NT) or 1x128 per column (K-grouped); in the K-grouped layout the
 scale group index is k/128 counted over the concatenated K axis; C is FP32 and only
@@ -94,6 +101,21 @@ def fp8_gemm_nt(a, sfa_words, b, sfb_words, c=None, rows=None) -> np.ndarray:
     return d
 
 
+def fp8_gemm_nn(a, sfa_words, b, sfb_words, c=None, rows=None) -> np.ndarray:
+    """D = C + A @ B with a [M, K] and b stored [K, N]."""
+    return fp8_gemm_nt(a, sfa_words, np.ascontiguousarray(b.T), sfb_words, c, rows)
+
+
+def fp8_gemm_tn(a, sfa_words, b, sfb_words, c=None, rows=None) -> np.ndarray:
+    """D = C + A @ B with a stored [K, M] and b stored [K, N]."""
+    return fp8_gemm_nt(np.ascontiguousarray(a.T), sfa_words, np.ascontiguousarray(b.T), sfb_words, c, rows)
+
+
+def fp8_gemm_tt(a, sfa_words, b, sfb_words, c=None, rows=None) -> np.ndarray:
+    """D = C + A @ B with a stored [K, M] and b stored [N, K]."""
+    return fp8_gemm_nt(np.ascontiguousarray(a.T), sfa_words, b, sfb_words, c, rows)
+
+
 # ---------------------------------------------------------------------------
 # M-grouped contiguous
 # ---------------------------------------------------------------------------
@@ -119,6 +141,12 @@ def m_grouped_fp8_gemm_nt_contiguous(a, sfa_words, b, sfb_words, m_indices, rows
         be = dequant_k_major(b[e], block_scales(sfb_words[e], n, k))
         d[sel] = dequant_k_major(a[src], sa[src]) @ be.T
     return d, written
+
+
+def m_grouped_fp8_gemm_nn_contiguous(a, sfa_words, b, sfb_words, m_indices, rows=None):
+    """As m_grouped_fp8_gemm_nt_contiguous with b stored [G, K, N]."""
+    return m_grouped_fp8_gemm_nt_contiguous(a, sfa_words, np.ascontiguousarray(np.transpose(b, (0, 2, 1))),
+                                            sfb_words, m_indices, rows)
 
 
 # ---------------------------------------------------------------------------

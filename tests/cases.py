@@ -125,3 +125,20 @@ def decode_out(arr: np.ndarray, out: str) -> np.ndarray:
     if out == "bf16":
         return F.bf16_to_f64(arr.view(np.uint16))
     return arr.astype(np.float64)
+
+
+# ----------------------------------------------------------- other layouts
+def layout_case(seed, layout, m, n, k, with_c, out="bf16"):
+    """A dense case with the operands stored in `layout` ("nn", "tn", "tt"): A as [K, M]
+    for a leading "t", B as [K, N] for a trailing "n" (same values as the NT case)."""
+    case = dense_case(seed, m, n, k, with_c, out)
+    a_t, b_n = layout[0] == "t", layout[1] == "n"
+    case["layout"] = layout
+    case["a_stored"] = np.ascontiguousarray(case["a"].T) if a_t else case["a"]
+    case["b_stored"] = np.ascontiguousarray(case["b"].T) if b_n else case["b"]
+    return case
+
+
+def layout_ref(case, rows=None):
+    fn = {"nn": oracle.fp8_gemm_nn, "tn": oracle.fp8_gemm_tn, "tt": oracle.fp8_gemm_tt}[case["layout"]]
+    return fn(case["a_stored"], case["sfa"], case["b_stored"], case["sfb"], case["c"], rows=rows)

@@ -66,6 +66,19 @@ def exact_dense(a, sfa, b, sfb, c, m, n) -> Fraction:
     return tot
 
 
+def exact_layout(a, sfa, b, sfb, c, m, n, a_t, b_n) -> Fraction:
+    """Element (m, n) with A stored [K][M] when a_t (else [M][K]) and B stored [K][N]
+    when b_n (else [N][K]); scales in the NT layouts."""
+    k = a.shape[0] if a_t else a.shape[1]
+    tot = Fraction(0) if c is None else Fraction(float(c[m, n]))
+    for kk in range(k):
+        g = kk // 128
+        av = a[kk, m] if a_t else a[m, kk]
+        bv = b[kk, n] if b_n else b[n, kk]
+        tot += fr_e4m3(av) * fr_ue8(word_byte(sfa, g, m)) * fr_e4m3(bv) * fr_ue8(word_byte(sfb, g, n // 128))
+    return tot
+
+
 def exact_k_grouped(a, sfa, b, sfb, ks, c, e, m, n) -> Fraction:
     off = int(sum(ks[:e]))
     tot = Fraction(0) if c is None else Fraction(float(c[e, m, n]))
@@ -123,6 +136,49 @@ def check_dense_brute_force(seed=0):
                 mag = sum(abs(fr_e4m3(a[i, kk]) * fr_e4m3(b[j, kk])) for kk in range(k)) * Fraction(2) ** 40
                 assert close_fp64(d[i, j], ex, mag, k), (m, n, k, i, j)
                 assert bits[i, j] == fr_to_bf16_bits(ex), (i, j)
+
+
+def check_layouts_brute_force(seed=5):
+    """NN, TN, TT against the exact sum read straight from the stored arrays; the square
+    case makes a transposition mistake silent in shape, so only the values can tell."""
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    fns = {"nn": (oracle.fp8_gemm_nn, False, True), "tn": (oracle.fp8_gemm_tn, True, True),
+           "tt": (oracle.fp8_gemm_tt, True, False)}
+    for name, (fn, a_t, b_n) in fns.items():
+        for (m, n, k, with_c) in [(128, 128, 128, False), (3, 130, 256, True)]:
+            a = rand_codes(g, (k, m) if a_t else (m, k))
+            b = rand_codes(g, (k, n) if b_n else (n, k))
+            sfa, sfb = rand_words(g, m, k // 128), rand_words(g, (n + 127) // 128, k // 128)
+            c = g.standard_normal((m, n)).astype(np.float32) if with_c else None
+            d = fn(a, sfa, b, sfb, c)
+            assert d.shape == (m, n), name
+            for i in (0, 1, m - 1):
+                for j in (0, 2, n - 1):
+                    ex = exact_layout(a, sfa, b, sfb, c, i, j, a_t, b_n)
+                    assert abs(Fraction(d[i, j]) - ex) <= (abs(ex) + 1) * Fraction(1, 2 ** 40), (name, m, n, i, j)
+
+
+def check_contiguous_nn_brute_force(seed=6):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, n, k = 2, 128, 128
+    m_indices = np.array([1, 1, -1, 0, 0, -1], dtype=np.int32)
+    m_total = len(m_indices)
+    a = rand_codes(g, (m_total, k))
+    b = rand_codes(g, (num_groups, k, n))          # [G][K][N]
+    sfa = rand_words(g, m_total, k // 128)
+    sfb = np.stack([rand_words(g, 1, k // 128) for _ in range(num_groups)])
+    d, written = oracle.m_grouped_fp8_gemm_nn_contiguous(a, sfa, b, sfb, m_indices)
+    assert list(written) == [e >= 0 for e in m_indices]
+    for i in range(m_total):
+        e = m_indices[i]
+        if e < 0:
+            assert np.all(np.isnan(d[i]))
+            continue
+        for j in (0, 5, n - 1):
+            ex = exact_layout(a, sfa, b[e], sfb[e], None, i, j, False, True)
+            assert abs(Fraction(d[i, j]) - ex) <= (abs(ex) + 1) * Fraction(1, 2 ** 40), (i, j)
 
 
 def check_contiguous_brute_force(seed=1):
@@ -255,6 +311,7 @@ def check_integer_valued():
     assert np.array_equal(d, (ai @ bi.T).astype(np.float64))
 
 
-ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_contiguous_brute_force,
+ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_force,
+              check_contiguous_nn_brute_force, check_contiguous_brute_force,
               check_masked_brute_force, check_k_grouped_brute_force, check_identity,
               check_one_hot, check_scale_probe, check_integer_valued]

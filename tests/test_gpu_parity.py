@@ -423,3 +423,71 @@ def test_pdl_dependent_launch_order(fg):
             assert np.array_equal(a, g.inner_bits())
     finally:
         fg.set_pdl(True)
+
+
+# ------------------------------------------------------- NN / TN / TT layouts
+def run_layout(fg, case, alias_c=False):
+    from gpu_util import GuardedOut, dev
+    out = GuardedOut(case["m"], case["n"], case["out"])
+    c_t = None
+    if case["c"] is not None:
+        if alias_c:
+            out.fill_from(case["c"])
+            c_t = out.tensor
+        else:
+            c_t = dev(case["c"])
+    fn = {"nn": fg.fp8_gemm_nn, "tn": fg.fp8_gemm_tn, "tt": fg.fp8_gemm_tt}[case["layout"]]
+    fn(dev(case["a_stored"]), dev(case["sfa"]), dev(case["b_stored"]), dev(case["sfb"]), out.tensor, c=c_t)
+    _status_ok(fg)
+    out.check_guards()
+    return out
+
+
+@pytest.mark.parametrize("layout,bn", [(lay, bn) for lay in ("nn", "tn", "tt") for bn in ("128", "256")]
+                         + [("tt", "224")])
+@pytest.mark.parametrize("m,n,k,with_c,out", [
+    (128, 256, 512, False, "bf16"),
+    (208, 272, 384, True, "f32"),         # ragged M and N tails, C
+    (64, 512, 1024, True, "f32"),         # one row block of 64 rows
+    (512, 400, 1280, False, "bf16"),      # several row blocks, N tail inside a 256 tile
+])
+def test_dense_layouts(fg, layout, bn, m, n, k, with_c, out, monkeypatch):
+    """fp8_gemm_{nn,tn,tt}: the same product with A stored [K, M] ("t") and/or B stored
+    [K, N] ("n"); MN-major operands go through 128-wide swizzle atoms in shared memory."""
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.layout_case(300 + m + n + k, layout, m, n, k, with_c, out)
+    C.compare(run_layout(fg, case).values(), C.layout_ref(case), f"{layout} BN={bn} {m}x{n}x{k}")
+
+
+def test_dense_layout_aliased_c(fg):
+    case = C.layout_case(41, "tn", 256, 384, 640, True, "f32")
+    C.compare(run_layout(fg, case, alias_c=True).values(), C.layout_ref(case), "tn aliased C")
+
+
+@pytest.mark.parametrize("layout", ["nn", "tn", "tt"])
+def test_layouts_match_nt_bit_for_bit(fg, layout, monkeypatch):
+    """Only the operand storage differs from NT (no K split): same values, same
+    accumulation order, so the FP32 outputs agree bit for bit."""
+    monkeypatch.setenv("FG_FORCE_SPLIT", "1")
+    case = C.layout_case(43, layout, 256, 512, 1024, True, "f32")
+    got = run_layout(fg, case).inner_bits()
+    nt = run_dense(fg, case).inner_bits()
+    assert np.array_equal(got, nt)
+
+
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_contiguous_nn_parity(fg, bn, monkeypatch):
+    """m_grouped_fp8_gemm_nn_contiguous: expert weights stored [G, K, N]."""
+    from gpu_util import GuardedOut, dev
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.contiguous_case(7, num_tokens=512, num_routed=16, topk=3, num_groups=5, n=384, k=384)
+    b_nn = np.ascontiguousarray(np.transpose(case["b"], (0, 2, 1)))
+    d = GuardedOut(case["m_total"], case["n"], "bf16")
+    fg.m_grouped_fp8_gemm_nn_contiguous(dev(case["a"]), dev(case["sfa"]), dev(b_nn), dev(case["sfb"]),
+                                        dev(case["m_indices"]), d.tensor)
+    _status_ok(fg)
+    d.check_guards()
+    ref, written = C.oracle.m_grouped_fp8_gemm_nn_contiguous(case["a"], case["sfa"], b_nn, case["sfb"],
+                                                             case["m_indices"])
+    assert np.array_equal(~d.is_sentinel(), written), "written row set differs"
+    C.compare(d.values()[written], ref[written], f"contiguous nn BN={bn}")

@@ -115,7 +115,27 @@ def _row_scale_transposed(sfa_words, mn, k):
     return s[::-1]
 
 
+def _nn_b_read_as_nt(a, sfa, b, sfb, c=None, rows=None):
+    return _orig_nt(a, sfa, b, sfb, c, rows)
+
+
+def _tt_a_read_as_nt(a, sfa, b, sfb, c=None, rows=None):
+    return _orig_nt(a, sfa, b, sfb, c, rows)
+
+
+def _tn_operands_swapped(a, sfa, b, sfb, c=None, rows=None):
+    return _orig_nt(np.ascontiguousarray(b.T), sfa, np.ascontiguousarray(a.T), sfb, c, rows)
+
+
+def _contig_nn_b_read_as_nt(a, sfa, b, sfb, m_indices, rows=None):
+    return _orig_contig(a, sfa, b, sfb, m_indices, rows)
+
+
 MUTANTS = {
+    "nn_b_not_transposed": [(G, "fp8_gemm_nn", lambda: _nn_b_read_as_nt)],
+    "tt_a_not_transposed": [(G, "fp8_gemm_tt", lambda: _tt_a_read_as_nt)],
+    "tn_operands_swapped": [(G, "fp8_gemm_tn", lambda: _tn_operands_swapped)],
+    "contiguous_nn_b_not_transposed": [(G, "m_grouped_fp8_gemm_nn_contiguous", lambda: _contig_nn_b_read_as_nt)],
     "e4m3_bias_8": [(F, "E4M3_TABLE", _bias8_table)],
     "e4m3_sign_dropped": [(F, "E4M3_TABLE", _unsigned_table)],
     "scale_bytes_reversed": [(G, "unpack_ue8m0", lambda: _unpack_reversed)],
