@@ -311,7 +311,84 @@ def check_integer_valued():
     assert np.array_equal(d, (ai @ bi.T).astype(np.float64))
 
 
+def check_silu_library():
+    """SiLU against a library routine (scipy's logistic expit) and its identities."""
+    from scipy.special import expit
+    from oracle import swiglu as S
+    x = np.concatenate([np.linspace(-60, 60, 20001), [0.0, 1e-300, -1e-300, 700.0, -700.0]])
+    got = S.silu(x)
+    want = x * expit(x)
+    assert np.all(np.abs(got - want) <= 4e-16 * np.maximum(np.abs(want), 1e-300))
+    assert S.silu(np.array([0.0]))[0] == 0.0
+    # silu(x) - silu(-x) = x * (sigma(x) + sigma(-x)) = x
+    y = np.linspace(-30, 30, 6001)
+    assert np.all(np.abs((S.silu(y) - S.silu(-y)) - y) <= 1e-14 * np.maximum(1.0, np.abs(y)))
+    # for x >= 64, exp(-x) is below half an ulp of 1: silu(x) == x exactly in FP64
+    z = np.arange(64.0, 200.0)
+    assert np.array_equal(S.silu(z), z)
+
+
+def check_swiglu_brute_force(seed=7):
+    """Contiguous gate-up GEMM + SwiGLU + requantisation on a tiny case: the GEMM element
+    exactly (rationals), SiLU from scipy's expit, then each code must be the E4M3 value
+    nearest to y / scale (half a spacing) and each scale the smallest admissible power of two."""
+    from scipy.special import expit
+    from oracle import swiglu as S
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, inter, k = 2, 128, 128
+    m_indices = np.array([1, -1, 0, 0], dtype=np.int32)
+    a = rand_codes(g, (len(m_indices), k))
+    b = rand_codes(g, (num_groups, 2 * inter, k))
+    sfa = rand_words(g, len(m_indices), k // 128)
+    sfb = np.stack([rand_words(g, 2, k // 128) for _ in range(num_groups)])
+    q, sf, written = S.m_grouped_fp8_gemm_nt_contiguous_swiglu(a, sfa, b, sfb, m_indices)
+    assert list(written) == [e >= 0 for e in m_indices]
+    for r, e in enumerate(m_indices):
+        if e < 0:
+            continue
+        h = np.array([float(exact_dense(a, sfa, b[e], sfb[e], None, r, j)) for j in range(2 * inter)])
+        y = (h[:inter] * expit(h[:inter]) * h[inter:]).astype(np.float32).astype(np.float64)
+        amax = Fraction(float(np.abs(y).max()))
+        scale = fr_ue8(int(sf[r, 0]))
+        assert amax <= 448 * scale and (amax == 0 or amax > 224 * scale), (r, float(amax), int(sf[r, 0]))
+        for j in range(inter):
+            t = Fraction(float(y[j])) / scale
+            code = fr_e4m3(int(q[r, j]))
+            mag = abs(t)
+            ex = max(mag.numerator.bit_length() - mag.denominator.bit_length(), -6) if mag else -6
+            if mag and Fraction(2) ** ex > mag:
+                ex -= 1
+            spacing = Fraction(2) ** (max(ex, -6) - 3)
+            assert abs(code - t) <= spacing / 2, (r, j, float(t), float(code))
+
+
+def check_swiglu_exact_probe():
+    """gate >= 64 makes SiLU(gate) == gate, so y = gate * up exactly (small integers): the
+    codes and scales then follow from exact arithmetic (torch's E4M3 cast as the library
+    rounding of y / scale)."""
+    import torch
+    from oracle import swiglu as S
+    g = np.random.Generator(np.random.PCG64(8))
+    gate = g.integers(64, 120, (5, 256)).astype(np.float64)
+    up = g.integers(-3, 4, (5, 256)).astype(np.float64)
+    q, sf = S.swiglu_quantize(np.concatenate([gate, up], axis=1))
+    y = gate * up
+    for r in range(5):
+        for grp in range(2):
+            seg = y[r, grp * 128:(grp + 1) * 128]
+            amax = Fraction(int(np.abs(seg).max()))
+            e = 0
+            while 448 * Fraction(2) ** e < amax:
+                e += 1
+            while e > -127 and amax and 448 * Fraction(2) ** (e - 1) >= amax:
+                e -= 1
+            assert int(sf[r, grp]) == (127 if amax == 0 else e + 127), (r, grp)
+            ref = torch.from_numpy(seg / 2.0 ** e).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(q[r, grp * 128:(grp + 1) * 128], ref), (r, grp)
+
+
 ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_force,
+              check_silu_library, check_swiglu_brute_force, check_swiglu_exact_probe,
               check_contiguous_nn_brute_force, check_contiguous_brute_force,
               check_masked_brute_force, check_k_grouped_brute_force, check_identity,
               check_one_hot, check_scale_probe, check_integer_valued]

@@ -131,7 +131,33 @@ def _contig_nn_b_read_as_nt(a, sfa, b, sfb, m_indices, rows=None):
     return _orig_contig(a, sfa, b, sfb, m_indices, rows)
 
 
+import oracle.swiglu as SW
+
+_orig_silu = SW.silu
+
+
+def _swiglu_halves_swapped(h):
+    h = np.asarray(h, dtype=np.float64)
+    i = h.shape[-1] // 2
+    return _orig_silu(h[..., i:]) * h[..., :i]
+
+
+def _sigmoid_not_silu(x):
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-x))
+
+
+def _silu_sign_flipped(x):
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(x))
+
+
 MUTANTS = {
+    "swiglu_halves_swapped": [(SW, "swiglu", lambda: _swiglu_halves_swapped)],
+    "silu_is_sigmoid": [(SW, "silu", lambda: _sigmoid_not_silu)],
+    "silu_sign_flipped": [(SW, "silu", lambda: _silu_sign_flipped)],
     "nn_b_not_transposed": [(G, "fp8_gemm_nn", lambda: _nn_b_read_as_nt)],
     "tt_a_not_transposed": [(G, "fp8_gemm_tt", lambda: _tt_a_read_as_nt)],
     "tn_operands_swapped": [(G, "fp8_gemm_tn", lambda: _tn_operands_swapped)],
