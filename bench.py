@@ -18,7 +18,8 @@ Two timed passes of --steps steps each:
      between consecutive GEMMs, which serialises them.
 
 Other workloads (--workload prefill | decode | contiguous | masked | k_grouped, and the
-other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn) time the
+other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn, and the fused
+gate-up GEMM contiguous_swiglu) time the
 single GEMMs on the same rules; they are measurement aids, the default line is the headline.
 
 Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
@@ -44,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_split.cu",
-                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu"]
+                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh"]
 
 
 def align4(x: int) -> int:
@@ -265,6 +266,7 @@ class Contiguous:
         self.d = torch.empty((m_total, n), dtype=torch.bfloat16, device="cuda")
         nv = int(counts.sum())
         used = int((counts > 0).sum())
+        self.nv, self.used = nv, used
         self.flops = 2.0 * nv * n * k
         self.bytes = (nv * k + used * n * k + self.sfa.numel() * 4 + self.sfb.numel() * 4 + nv * n * 2
                       + m_total * 4)
@@ -417,6 +419,36 @@ class PrefillTT(_PrefillLayout):
     description = "dense FP8 TT GEMM (A stored [K,M]) M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
 
 
+class ContiguousSwiGLU(Contiguous):
+    """The contiguous workload as the MoE gate-up GEMM with the fused SwiGLU + FP8
+    requantisation epilogue: B [32, 2 x 2048, 4096] (gate rows, then up rows), output
+    q [M_total, 2048] E4M3 + packed UE8M0 scales (the down projection's A operand)."""
+    name = "contiguous_swiglu"
+    description = ("M-grouped contiguous FP8 gate-up GEMM with fused SwiGLU + per-1x128 E4M3 requantisation: "
+                   "32 experts (top-6 of 8192 tokens, experts 0-31, 128-row padded segments), I=2048 (B 2I=4096 "
+                   "rows), K=4096; output E4M3 [M_total, 2048] + UE8M0 scales")
+
+    def __init__(self, torch, fg, seed):
+        super().__init__(torch, fg, seed)
+        m_total, inter = self.a.shape[0], self.b.shape[1] // 2
+        self.q = torch.empty((m_total, inter), dtype=torch.uint8, device="cuda")
+        self.sfq = torch.zeros((cdiv(inter, 512), align4(m_total)), dtype=torch.int32, device="cuda")
+        k, n2, nv = self.a.shape[1], self.b.shape[1], self.nv
+        self.bytes = (nv * k + self.used * n2 * k + self.sfa.numel() * 4 + self.sfb.numel() * 4
+                      + nv * inter + nv * (inter // 128) + m_total * 4)
+        self.parts = [{"name": "contiguous_swiglu", "flops": self.flops, "bytes": self.bytes}]
+        del self.d
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_gemm_nt_contiguous_swiglu(self.a, self.sfa, self.b, self.sfb,
+                                                                        self.m_indices, self.q, self.sfq)]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.m_indices)]
+        return ins, [(t, self.torch.empty_like(t, device="cpu").pin_memory()) for t in (self.q, self.sfq)]
+
+
 class ContiguousNN(Contiguous):
     """The contiguous workload with each expert's weights stored [K, N]."""
     name = "contiguous_nn"
@@ -433,7 +465,7 @@ class ContiguousNN(Contiguous):
 
 
 WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped, PrefillNN, PrefillTN,
-                                 PrefillTT, ContiguousNN)}
+                                 PrefillTT, ContiguousNN, ContiguousSwiGLU)}
 
 
 # ------------------------------------------------------------------- CPU oracle arm

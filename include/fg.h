@@ -131,6 +131,39 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G,
                                         void* d, int d_dtype, fg_stream_t stream);
 
 /*
+ * Gate-up GEMM of the MoE MLP with the SwiGLU and the FP8 requantisation of its output
+ * fused into the epilogue (the MoE MLP's linear 1 -> SwiGLU -> FP8 cast for linear 2:
+ * "Mega MoE", docsearch / README; MegaMoE DCU README "Runtime Routing", K2 "SwiGLU +
+ * channelwise FP8 quant").  Each group's weight b[g] holds I gate rows then I up rows:
+ *   h = A[m,:] @ b[g]^T  (g = m_indices[m]),   y[i] = SiLU(h[i]) * h[I + i],
+ *   SiLU(x) = x / (1 + exp(-x)),
+ * then per row and 1x128 group of y: scale 2^e, the smallest with amax <= 448 * 2^e, and
+ * q = E4M3 round-to-nearest-even of y * 2^-e (computed in FP32): exactly the A operand
+ * (and its sfa) of the down projection.
+ *   a    [M_total][K] E4M3, sfa [ceil(K/512)][align4(M_total)]
+ *   b    [G][2I][K]   E4M3, sfb [G][ceil(K/512)][align4(2I/128)] (128x128 blocks)
+ *   q    [M_total][I] E4M3 (out), sfq [ceil(I/512)][align4(M_total)] packed UE8M0 (out)
+ * Padding rows (m_indices == -1) are left untouched in q and sfq; only the bytes of sfq
+ * that name a computed group are written (the caller zeroes the rest if it reads them).
+ * I >= 128 and I % 128 == 0; the rest as fg_m_grouped_fp8_gemm_nt_contiguous.
+ */
+int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G,
+                                               const uint8_t* a, const int32_t* sfa,
+                                               const uint8_t* b, const int32_t* sfb,
+                                               const int32_t* m_indices,
+                                               uint8_t* q, int32_t* sfq, fg_stream_t stream);
+
+/* The same fused gate-up GEMM for the masked layout: a [G][M_max][K] with
+ * sfa [G][ceil(K/512)][align4(M_max)], b and sfb as above, masked_m as for
+ * fg_m_grouped_fp8_gemm_nt_masked; q [G][M_max][I], sfq [G][ceil(I/512)][align4(M_max)];
+ * rows >= masked_m[g] are left untouched. */
+int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K,
+                                           const uint8_t* a, const int32_t* sfa,
+                                           const uint8_t* b, const int32_t* sfb,
+                                           const int32_t* masked_m,
+                                           uint8_t* q, int32_t* sfq, fg_stream_t stream);
+
+/*
  * The same M-grouped contiguous GEMM with each group's weights stored N-major
  * (docsearch section 9 item 2, m_grouped_fp8_gemm_{nt, nn}_contiguous):
  *   D[m,:] = A[m,:] @ B[m_indices[m]],  b [G][K][N] E4M3 (N contiguous)

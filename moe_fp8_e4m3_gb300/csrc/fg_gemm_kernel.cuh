@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "fg_fp8.cuh"
 #include "fg_ptx.cuh"
 
 namespace fg {
@@ -95,6 +96,9 @@ struct GemmParams {
     int a_box_rows;        // rows of the A tensor-map box (128, or 64 when every tile has <= 64 rows)
     int pdl;               // host side: launch with programmatic stream serialisation
     int sfb_per_row;       // B scales: one per row of B and 1x128 K-group (else one per 128x128 block)
+    int32_t* sfq;          // SwiGLU epilogue: packed scale words of the quantised output
+    int sfq_ld;            //   int32 words per packed-word row (align4 of its rows)
+    long long sfq_gstride; //   words between groups (masked layout)
     long long b_gstride_k; // MN-major grouped B: rows of the [G*K][N] map between groups (K)
     int* status;
     unsigned long long timeout_ns;
@@ -418,7 +422,25 @@ __device__ __noinline__ bool split_k_tile(const SplitTile st, float* xb, uint32_
     return true;
 }
 
-template <int BN, int kMaj, bool k2Sm, bool kSplit>
+// SwiGLU variant (kSwiGLU): B holds each group's gate rows [0, N/2) and up rows
+// [N/2, N); output column block nb (128 wide) reads gate rows nb*128.. and up rows
+// N/2 + nb*128.. into one 256-row B tile, so the accumulator holds gate in columns
+// 0..127 and up in 128..255 of the same 128 outputs.  Returns the B-tile row of
+// tile row 0 of half h.
+__device__ __forceinline__ int swiglu_b_row(const GemmParams& p, const Tile& tl, int h) {
+    const int nb = tl.n0 / 256;
+    return (tl.b_coord - tl.n0) + (h ? p.N / 2 : 0) + nb * 128;
+}
+
+// SiLU(gate) * up of two FP32 accumulator words.  The fast division (<= 2 ulp) keeps
+// the epilogue short: the correctly rounded one took ~2x the whole GEMM's time; both are
+// far inside one E4M3 spacing of the requantised result.
+__device__ __forceinline__ float swiglu_value(uint32_t gate, uint32_t up) {
+    const float x = __uint_as_float(gate);
+    return __fdividef(x, 1.0f + __expf(-x)) * __uint_as_float(up);
+}
+
+template <int BN, int kMaj, bool k2Sm, bool kSplit, bool kSwiGLU>
 __global__ void __launch_bounds__(224, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_a = maps.a;
@@ -429,6 +451,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     static_assert(!(kMaj != kMajNT && k2Sm), "CTA pairs are used by the NT kernels only");
     static_assert(!(kSplit && (kMaj != kMajNT || k2Sm)), "split-K clusters are a dense NT variant");
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
+    static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !k2Sm && !kSplit),
+                  "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
     using C = TileCfg<BN, k2Sm>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -712,7 +736,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
                         const int kc = (tl.kb0 + kb) * 128;
                         mbar_arrive_expect_tx(fb, C::kBBytes);
-                        if constexpr (!kBmn) {
+                        if constexpr (kSwiGLU) {
+                            // B as [2G halves][I rows][K]: one box of the tile's 128 gate rows
+                            // and the matching 128 up rows (half 2g, then 2g + 1)
+                            tma_load_3d(sb, &tm_b, fb, kc, (tl.n0 / 256) * 128, 2 * tl.g);
+                        } else if constexpr (!kBmn) {
                             tma_load_2d(sb, &tm_b, fb, kc, tl.b_coord);
                         } else {   // B [K][N] (grouped: [G*K][N]): 128 (N) x 128 (K) boxes
                             const int krow = static_cast<int>(tl.b_krow) + kc;
@@ -740,7 +768,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 for (int i = 0; i < C::kSfbAtoms; ++i) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int n = tl.n0 + i * 128 + j * 32 + lane;
+                        int n = tl.n0 + i * 128 + j * 32 + lane;
+                        if constexpr (kSwiGLU) n = swiglu_b_row(p, tl, i) - (tl.b_coord - tl.n0) + j * 32 + lane;
                         const bool in = n < p.N;
                         cp_async_4(db + i * 512 + 4 * j, in ? pb + (p.sfb_per_row ? n : (n >> 7)) : pb, in ? 4u : 0u);
                     }
@@ -813,7 +842,91 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
         }
-        while (split == 1 && it.next(p, total_tiles, sched, cnt, tl)) {
+        if constexpr (kSwiGLU) {
+            // ------------------------------------------ SwiGLU + per-1x128 requantisation
+            // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
+            // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
+            // codes into this warp's slot (32 rows x 128 B, the TMA box) and a byte store of
+            // the scale into its packed word.  Two passes over TMEM: amax, then codes.
+            while (it.next(p, total_tiles, sched, cnt, tl)) {
+                const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+                if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
+                tc_fence_after();
+                const long long grow = tl.d_row + row;
+                bool row_ok = row < tl.valid_rows;
+                if (p.kind == kContiguous) {
+                    const int mi = __ldg(p.m_indices + grow);
+                    if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
+                    row_ok = (mi == tl.g);
+                }
+                const int nb = tl.n0 / 256;                      // 128-wide output column block
+                const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+                float amax = 0.0f;
+                if (tl.nkb > 0) {
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t g[32], u[32];
+                        tmem_ld_32x32b_x32(tacc + c0, g);
+                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
+                    }
+                }
+                const int e = scale_exponent(amax);
+                if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
+                __syncwarp();
+                uint8_t* rowp = slot0_ptr + lane * 128;
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t g[32], u[32];
+                    if (tl.nkb > 0) {
+                        tmem_ld_32x32b_x32(tacc + c0, g);
+                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
+                    }
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
+                        w[k] = word;
+                    }
+                    const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
+                    *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
+                if (row_ok) {
+                    const int sf_row = p.kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
+                    const int32_t* wp = p.sfq + (p.kind == kMasked ? tl.g * p.sfq_gstride : 0) +
+                                        (long long)(nb >> 2) * p.sfq_ld + sf_row;
+                    *(reinterpret_cast<uint8_t*>(const_cast<int32_t*>(wp)) + (nb & 3)) = static_cast<uint8_t>(e + 127);
+                }
+                // Dense rows past M are clipped by the TMA store; grouped layouts store only valid rows.
+                if (p.kind == kDense || __all_sync(0xffffffffu, row_ok)) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, slot0, nb * 128, tl.d_y + q * 32);
+                        bulk_commit_group();
+                    }
+                } else if (row_ok) {
+                    uint8_t* dst = static_cast<uint8_t*>(p.d) + grow * (p.N / 2) + nb * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(dst + 16 * j) = *reinterpret_cast<const uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                }
+                __syncwarp();
+                if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
+            }
+        }
+        while (!kSwiGLU && split == 1 && it.next(p, total_tiles, sched, cnt, tl)) {
             // warp-uniform decision before the .sync.aligned TMEM loads below
             const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
             if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }

@@ -1,0 +1,8 @@
+// fg_gemm_swiglu.cu - the gate-up GEMM with the fused SwiGLU + per-1x128 FP8
+// requantisation epilogue (NT, 256-row B tiles of 128 gate + 128 up rows), compiled in its
+// own translation unit.
+#include "fg_gemm_inst.cuh"
+
+namespace fg {
+template cudaError_t launch_gemm<256, kMajNT, false, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+}  // namespace fg

@@ -19,22 +19,12 @@
 #include <cstdint>
 
 #include "fg.h"
+#include "fg_fp8.cuh"
 
 namespace {
 
-__device__ __forceinline__ int scale_exponent(float amax) {
-    if (!(amax > 0.0f)) return 0;
-    int ex;
-    const float fr = frexpf(amax, &ex);     // amax = fr * 2^ex, fr in [0.5, 1)
-    // amax / 2^(ex-9) = 512 fr lies in [256, 512): within 448 iff fr <= 0.875
-    int e = fr <= 0.875f ? ex - 9 : ex - 8;
-    e = e < -127 ? -127 : (e > 127 ? 127 : e);
-    return e;
-}
-
-__device__ __forceinline__ uint32_t e4m3(float v) {
-    return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
+using fg::e4m3;
+using fg::scale_exponent;
 
 // One warp per (row, packed word): 512 consecutive K elements, 16 per lane, 8 lanes per
 // 128-group.

@@ -108,3 +108,28 @@ def test_k_grouped_full_size(fg, alias):
     ref = C.k_grouped_ref(case, rows=rows)
     for e in range(g_):
         C.compare(vals[e][rows], ref[e], f"k-grouped group {e} sampled rows")
+
+
+def test_contiguous_swiglu_full_size(fg):
+    """The fused gate-up GEMM at the contiguous benchmark shape read as gate + up
+    (8192 tokens, top-6 of 256, experts 0-31, B [32, 2 x 2048, 4096]): sampled valid rows
+    against the oracle, every padding row untouched."""
+    from gpu_util import dev
+    from oracle import swiglu as S
+    from test_gpu_swiglu import SENT_Q, _sf_bytes, _y_ref, compare_quantised
+    case = C.contiguous_case(1005)
+    m_total, inter = case["m_total"], case["n"] // 2
+    q = torch.full((m_total, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.zeros(((inter + 511) // 512, (m_total + 3) // 4 * 4), dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_gemm_nt_contiguous_swiglu(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                               dev(case["m_indices"]), q, sfq)
+    _ok(fg)
+    qh = q.cpu().numpy()
+    written = case["m_indices"] >= 0
+    assert np.all(qh[~written] == SENT_Q), "padding rows written"
+    g = np.random.Generator(np.random.PCG64(8))
+    rows = np.sort(g.choice(np.nonzero(written)[0], size=48, replace=False))
+    h, _ = C.contiguous_ref(case, rows=rows)
+    q_ref, sf_ref = S.swiglu_quantize(h)
+    sf = _sf_bytes(sfq.cpu().numpy(), m_total, inter // 128)[rows]
+    compare_quantised(qh[rows], sf, q_ref, sf_ref, _y_ref(h), "contiguous swiglu full size")
