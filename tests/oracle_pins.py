@@ -387,7 +387,52 @@ def check_swiglu_exact_probe():
             assert np.array_equal(q[r, grp * 128:(grp + 1) * 128], ref), (r, grp)
 
 
+def check_mqa_brute_force(seed=9):
+    """fp8_mqa_logits against exact rationals, element by element: the kv scale inside
+    the dot product, relu per head, the head weights, the [ks, ke) ranges (empty, full,
+    clipped past T) and -inf elsewhere."""
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    s_len, heads, dim, t_len = 4, 3, 8, 6
+    q = rand_codes(g, (s_len, heads, dim))
+    kv = rand_codes(g, (t_len, dim))
+    sf = (2.0 ** g.integers(-3, 4, t_len)).astype(np.float32)
+    w = g.standard_normal((s_len, heads)).astype(np.float32)
+    ks = np.array([0, 2, 3, 1]); ke = np.array([6, 5, 3, 9])
+    out = oracle.fp8_mqa_logits(q, kv, sf, w, ks, ke, clean_logits=True)
+    for i in range(s_len):
+        for j in range(t_len):
+            if not (ks[i] <= j < min(ke[i], t_len)):
+                assert out[i, j] == -np.inf, (i, j)
+                continue
+            tot = Fraction(0)
+            for h in range(heads):
+                dot = sum(fr_e4m3(q[i, h, d]) * fr_e4m3(kv[j, d]) * Fraction(float(sf[j])) for d in range(dim))
+                tot += max(dot, Fraction(0)) * Fraction(float(w[i, h]))
+            assert abs(Fraction(out[i, j]) - tot) <= (abs(tot) + 1) * Fraction(1, 2 ** 44), (i, j)
+    kept = oracle.fp8_mqa_logits(q, kv, sf, w, ks, ke, clean_logits=False)
+    assert np.isnan(kept[2]).all() and np.isnan(kept[0]).sum() == 0
+
+
+def check_mqa_closed_form():
+    """All-ones q and kv (0x38): every head's dot is D * sf[j] > 0, so
+    out[i, j] = D * sf[j] * sum_h w[i, h]; negating q (0xB8) makes every dot negative and
+    the logit exactly 0."""
+    import oracle
+    s_len, heads, dim, t_len = 3, 4, 16, 5
+    sf = np.array([1, 2, 0.5, 4, 0.25], np.float32)
+    w = np.arange(s_len * heads, dtype=np.float32).reshape(s_len, heads) - 3
+    ks, ke = np.zeros(s_len, int), np.full(s_len, t_len)
+    ones = oracle.fp8_mqa_logits(np.full((s_len, heads, dim), 0x38, np.uint8), np.full((t_len, dim), 0x38, np.uint8),
+                                 sf, w, ks, ke)
+    assert np.array_equal(ones, dim * sf[None, :].astype(np.float64) * w.sum(axis=1, dtype=np.float64)[:, None])
+    neg = oracle.fp8_mqa_logits(np.full((s_len, heads, dim), 0xB8, np.uint8), np.full((t_len, dim), 0x38, np.uint8),
+                                sf, w, ks, ke)
+    assert np.array_equal(neg, np.zeros_like(neg))
+
+
 ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_force,
+              check_mqa_brute_force, check_mqa_closed_form,
               check_silu_library, check_swiglu_brute_force, check_swiglu_exact_probe,
               check_contiguous_nn_brute_force, check_contiguous_brute_force,
               check_masked_brute_force, check_k_grouped_brute_force, check_identity,

@@ -154,7 +154,36 @@ def _silu_sign_flipped(x):
         return x / (1.0 + np.exp(x))
 
 
+import oracle.mqa as MQ
+
+
+def _mqa_no_relu(q, kv, kv_sf, weights, ks, ke, clean_logits=True, rows=None):
+    s_len, heads, dim = q.shape
+    t_len = kv.shape[0]
+    rows = np.arange(s_len) if rows is None else np.asarray(rows)
+    kvd = F.e4m3_to_f64(kv) * np.asarray(kv_sf, np.float64)[:, None]
+    out = np.full((len(rows), t_len), -np.inf if clean_logits else np.nan)
+    for r, i in enumerate(rows):
+        lo, hi = max(int(ks[i]), 0), min(int(ke[i]), t_len)
+        if hi > lo:
+            out[r, lo:hi] = (F.e4m3_to_f64(q[i]) @ kvd[lo:hi].T).T @ np.asarray(weights[i], np.float64)
+    return out
+
+
+def _mqa_range_inclusive(q, kv, kv_sf, weights, ks, ke, clean_logits=True, rows=None):
+    return _orig_mqa(q, kv, kv_sf, weights, ks, np.asarray(ke) + 1, clean_logits, rows)
+
+
+def _mqa_scale_dropped(q, kv, kv_sf, weights, ks, ke, clean_logits=True, rows=None):
+    return _orig_mqa(q, kv, np.ones_like(kv_sf), weights, ks, ke, clean_logits, rows)
+
+
+_orig_mqa = MQ.fp8_mqa_logits
+
 MUTANTS = {
+    "mqa_relu_dropped": [(MQ, "fp8_mqa_logits", lambda: _mqa_no_relu)],
+    "mqa_range_end_inclusive": [(MQ, "fp8_mqa_logits", lambda: _mqa_range_inclusive)],
+    "mqa_kv_scale_dropped": [(MQ, "fp8_mqa_logits", lambda: _mqa_scale_dropped)],
     "swiglu_halves_swapped": [(SW, "swiglu", lambda: _swiglu_halves_swapped)],
     "silu_is_sigmoid": [(SW, "silu", lambda: _sigmoid_not_silu)],
     "silu_sign_flipped": [(SW, "silu", lambda: _silu_sign_flipped)],
