@@ -19,7 +19,7 @@ Two timed passes of --steps steps each:
 
 Other workloads (--workload prefill | decode | contiguous | masked | k_grouped, and the
 other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn, and the fused
-gate-up GEMM contiguous_swiglu) time the
+gate-up GEMM contiguous_swiglu, and the indexer's mqa_logits) time the
 single GEMMs on the same rules; they are measurement aids, the default line is the headline.
 
 Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_split.cu",
-                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh"]
+                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh", "fg_mqa.cu"]
 
 
 def align4(x: int) -> int:
@@ -449,6 +449,49 @@ class ContiguousSwiGLU(Contiguous):
         return ins, [(t, self.torch.empty_like(t, device="cpu").pin_memory()) for t in (self.q, self.sfq)]
 
 
+class MqaLogits:
+    """Lightning-indexer MQA logits (non-paged): 4096 query tokens x 4096 kv tokens, causal
+    ranges (token i sees kv [0, i]), 64 heads, D = 128, clean_logits; FP32 out [4096, 4096].
+    Tensor-bound: 137 GFLOP of FP8 products against ~100 MB of traffic."""
+    name = "mqa_logits"
+    description = ("FP8 MQA logits: S=4096 query x T=4096 kv tokens, causal ranges, H=64 heads, D=128, "
+                   "kv per-token FP32 scales, clean_logits; FP32 logits [4096, 4096]")
+    S, T, H, D = 4096, 4096, 64, 128
+
+    def __init__(self, torch, fg, seed):
+        import workloads
+        self.torch, self.fg = torch, fg
+        s_len, t_len, heads, dim = self.S, self.T, self.H, self.D
+        xq = workloads.device_normal(seed, (s_len * heads, dim))
+        self.q = torch.empty((s_len * heads, dim), dtype=torch.uint8, device="cuda")
+        sfq = torch.zeros((cdiv(dim, 512), align4(s_len * heads)), dtype=torch.int32, device="cuda")
+        fg.quantize_1x128_rows(xq, self.q, sfq)     # E4M3 codes; the per-row scales are not used
+        self.q = self.q.view(s_len, heads, dim)
+        xk = workloads.device_normal(seed + 1, (t_len, dim))
+        self.kv = torch.empty((t_len, dim), dtype=torch.uint8, device="cuda")
+        sfk = torch.zeros((1, align4(t_len)), dtype=torch.int32, device="cuda")
+        fg.quantize_1x128_rows(xk, self.kv, sfk)
+        self.kv_sf = torch.ldexp(torch.ones(t_len, device="cuda"),
+                                 (sfk[0, :t_len] & 0xFF).to(torch.int32) - 127).float()
+        del xq, xk
+        self.w = workloads.device_normal(seed + 2, (s_len, heads))
+        self.ks = torch.zeros(s_len, dtype=torch.int32, device="cuda")
+        self.ke = torch.arange(1, s_len + 1, dtype=torch.int32, device="cuda")
+        self.out = torch.empty((s_len, t_len), dtype=torch.float32, device="cuda")
+        pairs = s_len * (s_len + 1) // 2
+        self.flops = 2.0 * pairs * heads * dim
+        self.bytes = s_len * heads * dim + t_len * dim + t_len * 4 + s_len * heads * 4 + 2 * s_len * 4 + s_len * t_len * 4
+        self.parts = [{"name": "mqa_logits", "flops": self.flops, "bytes": self.bytes, "bound": "tensor"}]
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda: self.fg.fp8_mqa_logits(self.q, self.kv, self.kv_sf, self.w, self.ks, self.ke, self.out)]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.q, self.kv, self.kv_sf, self.w, self.ks, self.ke)]
+        return ins, [(self.out, self.torch.empty_like(self.out, device="cpu").pin_memory())]
+
+
 class ContiguousNN(Contiguous):
     """The contiguous workload with each expert's weights stored [K, N]."""
     name = "contiguous_nn"
@@ -465,7 +508,7 @@ class ContiguousNN(Contiguous):
 
 
 WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped, PrefillNN, PrefillTN,
-                                 PrefillTT, ContiguousNN, ContiguousSwiGLU)}
+                                 PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
 
 
 # ------------------------------------------------------------------- CPU oracle arm
@@ -644,10 +687,17 @@ def run_gpu(args):
                    "timing": "step: events at step boundaries only; kernels: a second pass with an event "
                              "after every GEMM",
                    "kernels": kernels},
-        "roofline": {"bound": "hbm", "kernel": part["name"], "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": part["bytes"],
-                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"},
+        "roofline": ({"bound": "hbm", "kernel": part["name"], "achieved": round(achieved, 1),
+                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                      "traffic": traffic, "algorithmic_bytes_per_launch": part["bytes"],
+                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"}
+                     if part.get("bound", "hbm") == "hbm" else
+                     {"bound": "tensor", "kernel": part["name"],
+                      "achieved": round(part["flops"] / (per_kernel[dom] * 1e-3) / 1e12, 1),
+                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                      "frac": round(part["flops"] / (per_kernel[dom] * 1e-3) / 1e12 / fp8_peak, 4),
+                      "traffic": traffic, "algorithmic_flops_per_launch": part["flops"],
+                      "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal fp8/bf16 ratio)"}),
         "roofline_tensor": {"kernel": part["name"],
                             "achieved": round(part["flops"] / (per_kernel[dom] * 1e-3) / 1e12, 1),
                             "peak": round(fp8_peak, 1), "unit": "TFLOP/s",

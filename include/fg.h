@@ -251,6 +251,22 @@ int fg_quantize_128x128_blocks(int G, int N, int K, const float* w, uint8_t* q, 
 int fg_quantize_1x128_cols(int K, int MN, const float* x, uint8_t* q, int32_t* sf,
                            fg_stream_t stream);
 
+/*
+ * MQA logits of the lightning indexer, non-paged (docsearch section 11 "Use V3.2 MQA
+ * Kernels for Indexers", fp8_mqa_logits): for query token i and every kv token j in
+ * [ks[i], ke[i]) (clipped to [0, T)),
+ *   out[i, j] = sum_h relu(q[i, h, :] . (kv[j, :] * kv_sf[j])) * weights[i, h]
+ * computed with FP32 accumulation; with clean_logits != 0 every other entry of out is
+ * -inf, otherwise those entries are left untouched.
+ *   q        [S][H][D]  E4M3          kv       [T][D] E4M3      kv_sf [T] FP32
+ *   weights  [S][H]     FP32          ks, ke   [S] int32 (device)
+ *   out      [S][T]     FP32
+ * Supported: H == 64 and D == 128 (FG_ERR_UNSUPPORTED otherwise); S >= 0, T >= 1.
+ */
+int fg_fp8_mqa_logits(int S, int T, int H, int D, const uint8_t* q, const uint8_t* kv,
+                      const float* kv_sf, const float* weights, const int32_t* ks,
+                      const int32_t* ke, int clean_logits, float* out, fg_stream_t stream);
+
 /* Row alignment of each group segment in the contiguous layout: 128, the M block
  * (docsearch section 9 item 2 and section 10). */
 int fg_get_mk_alignment_for_contiguous_layout(void);

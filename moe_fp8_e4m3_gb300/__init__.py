@@ -33,6 +33,7 @@ _SIGNATURES = {
     "fg_m_grouped_fp8_gemm_nt_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_gemm_nn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_gemm_nt_contiguous_swiglu": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fg_fp8_mqa_logits": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked_swiglu": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
     "fg_k_grouped_fp8_gemm_tn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -183,6 +184,20 @@ def m_grouped_fp8_gemm_nt_masked_swiglu(a, sfa, b, sfb, masked_m, q, sfq, stream
     _check(lib.fg_m_grouped_fp8_gemm_nt_masked_swiglu(g, m_max, n2 // 2, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb),
                                                       _ptr(masked_m), _ptr(q), _ptr(sfq), _stream(stream)),
            "m_grouped_fp8_gemm_nt_masked_swiglu")
+
+
+def fp8_mqa_logits(q, kv, kv_sf, weights, ks, ke, out, clean_logits=True, stream=None) -> None:
+    """Lightning-indexer MQA logits.  q [S,H,D] E4M3 (H=64, D=128); kv [T,D] E4M3;
+    kv_sf float32 [T]; weights float32 [S,H]; ks, ke int32 [S]; out float32 [S,T]."""
+    import torch
+    _fp8(q, "q"); _fp8(kv, "kv"); _i32(ks, "ks"); _i32(ke, "ke")
+    for t, name in ((kv_sf, "kv_sf"), (weights, "weights"), (out, "out")):
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise TypeError(f"{name} must be a contiguous CUDA float32 tensor")
+    s_len, heads, dim = q.shape
+    t_len = kv.shape[0]
+    _check(lib.fg_fp8_mqa_logits(s_len, t_len, heads, dim, _ptr(q), _ptr(kv), _ptr(kv_sf), _ptr(weights), _ptr(ks),
+                                 _ptr(ke), 1 if clean_logits else 0, _ptr(out), _stream(stream)), "fp8_mqa_logits")
 
 
 def m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, d, stream=None) -> None:

@@ -14,6 +14,7 @@
 
 #include "fg.h"
 #include "fg_launch.h"
+#include "fg_mqa.cuh"
 
 // Device status word: first contract violation or wait time-out since the last read.
 __device__ int g_fg_status = 0;
@@ -693,6 +694,44 @@ int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_masked_swiglu G=%d M_max=%d I=%d K=%d grid=%d\n", G, M_max, I, K, grid);
     return launch_swiglu(p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fg_fp8_mqa_logits(int S, int T, int H, int D, const uint8_t* q, const uint8_t* kv, const float* kv_sf,
+                      const float* weights, const int32_t* ks, const int32_t* ke, int clean_logits, float* out,
+                      fg_stream_t stream) {
+    if (S < 0 || T < 1 || H < 1 || D < 1) return FG_ERR_INVALID_ARG;
+    if (H != 64 || D != 128) return FG_ERR_UNSUPPORTED;
+    if ((long long)S * H > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
+    if (!q || !kv || !kv_sf || !weights || !ks || !ke || !out) return FG_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kv) || !aligned4(kv_sf) || !aligned4(weights) || !aligned4(ks) ||
+        !aligned4(ke) || !aligned4(out))
+        return FG_ERR_INVALID_ARG;
+    if (S == 0) return FG_OK;
+    DeviceState* st = nullptr;
+    int rc;
+    if ((rc = device_state(&st))) return rc;
+    const int sms = sms_in_use(*st);
+    fg::MqaParams p{};
+    p.S = S; p.T = T;
+    p.kv_sf = kv_sf; p.weights = weights; p.ks = ks; p.ke = ke; p.out = out;
+    p.clean = clean_logits ? 1 : 0;
+    p.status = st->status;
+    p.timeout_ns = g_timeout_ns;
+    p.pdl = g_pdl;
+    fg::MqaMaps mm;
+    std::memset(&mm, 0, sizeof(mm));
+    if (!encode_2d(&mm.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 128, (uint64_t)S * 64, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mm.kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, kv, 128, (uint64_t)T, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FG_ERR_INVALID_ARG;
+    const int pairs = (S + 1) / 2;
+    const int grid = pairs < sms ? pairs : sms;
+    if (print_configs())
+        std::fprintf(stderr, "[fg] fp8_mqa_logits S=%d T=%d H=%d D=%d clean=%d grid=%d\n", S, T, H, D, p.clean, grid);
+    if (fg::launch_mqa(p, mm, grid, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    return FG_OK;
 }
 
 int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const uint8_t* a,

@@ -133,3 +133,13 @@ def test_contiguous_swiglu_full_size(fg):
     q_ref, sf_ref = S.swiglu_quantize(h)
     sf = _sf_bytes(sfq.cpu().numpy(), m_total, inter // 128)[rows]
     compare_quantised(qh[rows], sf, q_ref, sf_ref, _y_ref(h), "contiguous swiglu full size")
+
+
+def test_mqa_logits_full_size(fg):
+    """Causal MQA logits at the benchmark size (4096 query x 4096 kv tokens, 64 heads,
+    D = 128): sampled query rows against the oracle, -inf above the diagonal."""
+    from test_gpu_mqa import check, mqa_case, run
+    case = mqa_case(1006, 4096, 4096, "causal")
+    got = run(fg, case, True)
+    rows = _rows(4096, 24, 9)
+    check(case, got, True, rows=rows)
