@@ -596,12 +596,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
                         const int kc = (tl.kb0 + kb) * 128;
                         if constexpr (k2Sm) {
-                            const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
-                            // both CTAs' tiles complete on the leader's barrier
+                            // both CTAs' tiles complete on the leader's barrier; B comes from
+                            // the scale-loader warp
                             if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kABytes + C::kBBytes));
-                            const uint32_t fbl = map_shared_rank(fb, 0);
-                            tma_load_2d_pair(sa, &tm_a, fbl, kc, tl.a_coord);
-                            tma_load_2d_pair(sb, &tm_b, fbl, kc, tl.b_coord);
+                            tma_load_2d_pair(sa, &tm_a, map_shared_rank(fb, 0), kc, tl.a_coord);
                         } else if (!kAmn) {   // B is loaded by the scale-loader warp
                             mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
@@ -730,7 +728,13 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 // warp-uniform decision: every lane leaves together on abort
                 const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                if constexpr (!k2Sm) {
+                if constexpr (k2Sm) {
+                    // this CTA's half of B, completing on the leader's barrier (armed by its producer)
+                    if (lane == 0)
+                        tma_load_2d_pair(sbase + C::kOffB + s * C::kBBytes, &tm_b, map_shared_rank(full_bar(s), 0),
+                                         (tl.kb0 + kb) * 128, tl.b_coord);
+                    __syncwarp();
+                } else {
                     if (lane == 0) {
                         const uint32_t fb = full_bar(s);
                         const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
