@@ -142,3 +142,35 @@ def layout_case(seed, layout, m, n, k, with_c, out="bf16"):
 def layout_ref(case, rows=None):
     fn = {"nn": oracle.fp8_gemm_nn, "tn": oracle.fp8_gemm_tn, "tt": oracle.fp8_gemm_tt}[case["layout"]]
     return fn(case["a_stored"], case["sfa"], case["b_stored"], case["sfb"], case["c"], rows=rows)
+
+
+# ------------------------------------------------------------- MQA logits
+def mqa_case(seed, s_len, t_len, ranges="random", heads=64, dim=128):
+    """Indexer inputs: q encoded to E4M3 as drawn (clipped to the E4M3 range); each key row
+    x_t scaled by sf_t = amax_t / 448 (FP32) and encoded, so kv * sf restores x_t."""
+    w = workloads.mqa(seed, s_len, t_len, heads, dim, ranges)
+    q = F.f64_to_e4m3(np.clip(w["q"], -448, 448))
+    sf = (np.abs(w["x"]).max(axis=1) / 448.0).astype(np.float32)
+    kv = F.f64_to_e4m3(w["x"] / sf[:, None].astype(np.float64))
+    return {"q": q, "kv": kv, "sf": sf, "w": w["w"], "ks": w["ks"], "ke": w["ke"]}
+
+
+# ---------------------------------------------------- quantised SwiGLU output
+def dequant_1x128(q, sf):
+    """codes [R, I], scale bytes [R, I/128] -> float64 [R, I]"""
+    return F.e4m3_to_f64(q) * np.repeat(F.ue8m0_to_f64(sf), 128, axis=1)
+
+
+def compare_quantised(q, sf, q_ref, sf_ref, y_ref, what):
+    """q, sf: kernel codes / scale bytes of the valid rows; *_ref: the oracle's; y_ref: the
+    oracle's FP32-rounded SwiGLU values (before quantisation)."""
+    assert q.shape == q_ref.shape and sf.shape == sf_ref.shape
+    got, ref = dequant_1x128(q, sf), dequant_1x128(q_ref, sf_ref)
+    scale = np.repeat(F.ue8m0_to_f64(np.maximum(sf, sf_ref)), 128, axis=1)
+    rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
+    bound = 0.126 * np.abs(y_ref) + 2.0 ** -9 * scale + 1e-5 * rms
+    err = np.abs(got - ref)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} outputs off by more than one E4M3 spacing"
+    assert np.mean(q == q_ref) >= 0.99, f"{what}: only {np.mean(q == q_ref):.4f} of codes identical"
+    assert np.mean(sf == sf_ref) >= 0.99, f"{what}: only {np.mean(sf == sf_ref):.4f} of scales identical"

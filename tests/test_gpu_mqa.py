@@ -7,7 +7,6 @@ import numpy as np
 import pytest
 
 import cases as C
-from oracle import formats as F
 from oracle import mqa as MQ
 
 pytestmark = pytest.mark.gpu
@@ -30,26 +29,7 @@ def _ok(fg):
     assert st == 0, (st, hex(detail))
 
 
-def mqa_case(seed, s_len, t_len, ranges="random"):
-    g = np.random.Generator(np.random.PCG64(seed))
-    q = F.f64_to_e4m3(np.clip(g.standard_normal((s_len, H, D)) * 4, -448, 448))
-    x = g.standard_normal((t_len, D))
-    amax = np.abs(x).max(axis=1)
-    sf = (amax / 448.0).astype(np.float32)
-    kv = F.f64_to_e4m3(x / sf[:, None].astype(np.float64))
-    w = g.standard_normal((s_len, H)).astype(np.float32)
-    if ranges == "causal":
-        ks = np.zeros(s_len, np.int32)
-        ke = (np.arange(s_len) + 1 + (t_len - s_len)).astype(np.int32)
-    else:
-        a = g.integers(-5, t_len + 5, s_len)
-        b = g.integers(-5, t_len + 40, s_len)
-        ks, ke = np.minimum(a, b).astype(np.int32), np.maximum(a, b).astype(np.int32)
-        ks[0], ke[0] = 0, t_len            # full
-        if s_len > 2:
-            ks[1], ke[1] = 7, 7            # empty
-            ks[2], ke[2] = t_len - 3, t_len + 100   # clipped past T
-    return {"q": q, "kv": kv, "sf": sf, "w": w, "ks": ks, "ke": ke}
+mqa_case = C.mqa_case
 
 
 def run(fg, case, clean=True):

@@ -36,24 +36,7 @@ def _ok(fg):
     assert st == 0, (st, hex(detail))
 
 
-def _dequant(q, sf):
-    """codes [R, I], scale bytes [R, I/128] -> float64 [R, I]"""
-    return F.e4m3_to_f64(q) * np.repeat(F.ue8m0_to_f64(sf), 128, axis=1)
-
-
-def compare_quantised(q, sf, q_ref, sf_ref, y_ref, what):
-    """q, sf: kernel codes / scale bytes of the valid rows; *_ref: the oracle's; y_ref: the
-    oracle's FP32-rounded SwiGLU values (before quantisation)."""
-    assert q.shape == q_ref.shape and sf.shape == sf_ref.shape
-    got, ref = _dequant(q, sf), _dequant(q_ref, sf_ref)
-    scale = np.repeat(F.ue8m0_to_f64(np.maximum(sf, sf_ref)), 128, axis=1)
-    rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
-    bound = 0.126 * np.abs(y_ref) + 2.0 ** -9 * scale + 1e-5 * rms
-    err = np.abs(got - ref)
-    bad = err > bound
-    assert not bad.any(), f"{what}: {int(bad.sum())} outputs off by more than one E4M3 spacing"
-    assert np.mean(q == q_ref) >= 0.99, f"{what}: only {np.mean(q == q_ref):.4f} of codes identical"
-    assert np.mean(sf == sf_ref) >= 0.99, f"{what}: only {np.mean(sf == sf_ref):.4f} of scales identical"
+compare_quantised = C.compare_quantised
 
 
 def _sf_bytes(words, rows, groups):

@@ -20,6 +20,10 @@ Workloads (shapes and distributions of the five benchmark cases):
               random scale bytes; B[G,N,K] ~ N(0, 0.02).
 * k-grouped:  per-expert K lengths ~ Multinomial(K_sum, uniform), each padded up to a
               multiple of 128 with zero rows; A[K,M], B[K,N] ~ N(0,1); C[G,M,N] ~ N(0,1).
+* mqa:        indexer queries q[S,H,D] ~ N(0, 16), keys x[T,D] ~ N(0,1), head weights
+              w[S,H] ~ N(0,1); per-token kv ranges either causal (token i of S sees the
+              last T-S+i+1 keys' prefix) or random, with a full, an empty and a
+              clipped-past-T range planted in rows 0, 1, 2.
 """
 from __future__ import annotations
 
@@ -124,6 +128,25 @@ def k_grouped(seed: int, num_groups: int = 8, m: int = 4096, n: int = 2048,
         off += int(ks_pad[e])
     return {"a": a, "b": b, "ks": ks_pad.astype(np.int32), "ks_true": ks_true,
             "c": _normal(g, (num_groups, m, n))}
+
+
+def mqa(seed: int, s_len: int, t_len: int, heads: int = 64, dim: int = 128, ranges: str = "random") -> dict:
+    g = rng(seed)
+    q = g.standard_normal((s_len, heads, dim)) * 4.0
+    x = g.standard_normal((t_len, dim))
+    w = g.standard_normal((s_len, heads)).astype(np.float32)
+    if ranges == "causal":
+        ks = np.zeros(s_len, np.int32)
+        ke = (np.arange(s_len) + 1 + (t_len - s_len)).astype(np.int32)
+    else:
+        lo = g.integers(-5, t_len + 5, s_len)
+        hi = g.integers(-5, t_len + 40, s_len)
+        ks, ke = np.minimum(lo, hi).astype(np.int32), np.maximum(lo, hi).astype(np.int32)
+        ks[0], ke[0] = 0, t_len
+        if s_len > 2:
+            ks[1], ke[1] = 7, 7
+            ks[2], ke[2] = t_len - 3, t_len + 100
+    return {"q": q, "x": x, "w": w, "ks": ks, "ke": ke}
 
 
 def device_normal(seed: int, shape, std: float = 1.0, device: str = "cuda"):
