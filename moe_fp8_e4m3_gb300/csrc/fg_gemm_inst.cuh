@@ -11,7 +11,7 @@ namespace fg {
 // Raises the kernel's dynamic shared-memory limit once per device.
 template <int BN, int kMaj, bool k2Sm, bool kSplit, bool kSwiGLU>
 cudaError_t configure_gemm() {
-    constexpr int kSmem = TileCfg<BN, k2Sm>::kSmemBytes;
+    constexpr int kSmem = TileCfg<BN, k2Sm, kSplit>::kSmemBytes;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -54,7 +54,7 @@ cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cud
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(224);
-    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm>::kSmemBytes;
+    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm, kSplit>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, k2Sm ? 2 : (kSplit ? p.split : 1), p.pdl != 0);
@@ -68,7 +68,7 @@ cudaError_t max_active_clusters(int cluster, int* out) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
     cfg.blockDim = dim3(224);
-    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm>::kSmemBytes;
+    cfg.dynamicSmemBytes = TileCfg<BN, k2Sm, kSplit>::kSmemBytes;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, cluster, false);
     return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kMaj, k2Sm, kSplit, kSwiGLU>, &cfg);

@@ -17,10 +17,12 @@
 // picks byte (g mod 4).
 //
 // Warp roles (224 threads):
-//   warp 0      TMA producer: A and B tiles into a ring of shared-memory stages
+//   warp 0      TMA producer: A tiles into a ring of shared-memory stages
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
 //   warp 2      scale loader: packed UE8M0 words copied by cp.async into the tcgen05.cp
-//               layout of each stage, completion tracked by the stage's mbarrier
+//               layout of each stage, completion tracked by the stage's mbarrier; lane 0
+//               also issues the stage's B tile (a warp's TMA loads complete one after
+//               another, so A and B come from different warps)
 //   warps 3..6  epilogue: TMEM -> registers, + C (TMA-prefetched into shared memory),
 //               -> BF16/FP32 -> swizzled shared-memory slot -> TMA store
 // Accumulators are double-buffered in TMEM when two fit next to the scale slots
@@ -105,7 +107,7 @@ struct GemmParams {
     int debug_stall;
 };
 
-template <int BN, bool k2Sm = false>
+template <int BN, bool k2Sm = false, bool kSplit = false>
 struct TileCfg {
     static constexpr int kBM = 128, kBK = 128;
     static constexpr int kSfbAtoms = (BN + 127) / 128;
@@ -122,7 +124,9 @@ struct TileCfg {
     // Epilogue: per warp, kSlots shared-memory slots of 32 rows x 128 bytes.
     // C-prefetch depth against pipeline stages: wide tiles keep four slots per warp (their
     // epilogue streams the most C), narrow tiles and CTA pairs take more stages instead.
-    static constexpr int kSlots = k2Sm ? 2 : (BN >= 256 ? 1 : (BN >= 192 ? 4 : 2));
+    // Split-K variants exchange through the operand ring and need no slots: their shared
+    // memory goes to pipeline stages.
+    static constexpr int kSlots = kSplit ? 0 : (k2Sm ? 2 : (BN >= 256 ? 1 : (BN >= 192 ? 4 : 2)));
     static constexpr int kSlotBytes = 4096;
     static constexpr int kEpiBytes = 4 * kSlots * kSlotBytes;
     static constexpr int kMiscBytes = 1024 + 2 * (kMaxGroups + 1) * 4;   // barriers etc. + group tables
@@ -453,7 +457,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
     static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !k2Sm && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
-    using C = TileCfg<BN, k2Sm>;
+    using C = TileCfg<BN, k2Sm, kSplit>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -494,7 +498,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             mbar_init(acce_bar(b), k2Sm && leader ? 8 : 4);   // one arrive per epilogue warp (of both CTAs)
         }
         mbar_init(mma_drain_bar, 1);
-        for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
+        if constexpr (C::kSlots > 0)
+            for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
         mbar_init(xfull_bar, 4 * split);   // split-K: every epilogue warp of the cluster
         *abort_flag = 0;
         fence_mbar_init();
@@ -505,8 +510,23 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
         tma_prefetch_map(&tm_d);
         if (p.has_c) tma_prefetch_map(&tm_c);
     }
-    // Nothing above touched global memory (the tensor maps are kernel parameters): under a
-    // programmatic launch this is where the previous grid's results become visible.
+    if (warp == 1) {
+        if constexpr (k2Sm) {   // collective: one warp of each CTA of the pair
+            tmem_alloc_pair(smem_u32(tmem_slot), 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), 512);
+            tmem_relinquish();
+        }
+    }
+    tc_fence_before();
+    // the cluster's barriers are initialised before any CTA of it arrives on them remotely
+    if (k2Sm || split > 1) cluster_sync();
+    else __syncthreads();
+    tc_fence_after();
+    // Nothing above touched global memory (the tensor maps are kernel parameters), so the
+    // set-up overlaps the previous grid's tail under a programmatic launch; here its results
+    // become visible.
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_launch_dependents();
     // Group tables for the masked (tile prefix) and K-grouped (K-group prefix) layouts.
@@ -550,20 +570,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             }
         }
     }
-    if (warp == 1) {
-        if constexpr (k2Sm) {   // collective: one warp of each CTA of the pair
-            tmem_alloc_pair(smem_u32(tmem_slot), 512);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(tmem_slot), 512);
-            tmem_relinquish();
-        }
-    }
-    tc_fence_before();
-    // the cluster's barriers are initialised before any CTA of it arrives on them remotely
-    if (k2Sm || split > 1) cluster_sync();
-    else __syncthreads();
-    tc_fence_after();
+    if (p.kind == kMasked || p.kind == kKGrouped) __syncthreads();   // the group tables
     const uint32_t tmem_base = *tmem_slot;
     if (p.kind == kMasked) total_tiles = sched[p.G];
     if (p.kind == kKGrouped) total_tiles = sched[p.G] < 0 ? 0 : p.G * p.num_mb * p.num_nb;
@@ -800,35 +807,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
         uint8_t* slot0_ptr = smem + C::kOffEpi + ew * C::kSlots * C::kSlotBytes;
         const bool kg = p.kind == kKGrouped;
 
-        // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
-        TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank, split);
-        Tile ctl;
-        bool c_have = (p.has_c && split == 1) ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
-        int c_chunk = 0;
-        uint32_t c_issued = 0;       // chunks whose C load has been issued
-        auto issue_c = [&](uint32_t chunk_id) {
-            // chunk_id-th chunk of this warp's stream goes to slot chunk_id % kSlots
-            const int nch = (min(BN, p.N - ctl.n0) + 31) / 32;
-            const int sl = static_cast<int>(chunk_id % C::kSlots);
-            const uint32_t dst = slot0 + sl * C::kSlotBytes;
-            const uint32_t bar = cfull_bar(ew, sl);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, C::kSlotBytes);
-            const int x = ctl.n0 + c_chunk * 32;
-            if (kg) tma_load_3d(dst, &tm_c, bar, x, ctl.d_y + q * 32, ctl.d_z);
-            else tma_load_2d(dst, &tm_c, bar, x, ctl.d_y + q * 32);
-            if (++c_chunk == nch) {
-                c_chunk = 0;
-                c_have = cit.next(p, total_tiles, sched, cnt, ctl);
-            }
-        };
-        if (lane == 0) {
-            while (c_have && c_issued + 1 < static_cast<uint32_t>(C::kSlots)) issue_c(c_issued++);
-        }
-
         int acc = 0;
         uint32_t acc_ph = 0;
-        uint32_t chunk_id = 0;       // chunks consumed so far
         bool aborted = false;
         TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile tl;
@@ -845,15 +825,121 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 x_ph ^= 1u;
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
-        }
-        if constexpr (kSwiGLU) {
-            // ------------------------------------------ SwiGLU + per-1x128 requantisation
-            // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
-            // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
-            // codes into this warp's slot (32 rows x 128 B, the TMA box) and a byte store of
-            // the scale into its packed word.  Two passes over TMEM: amax, then codes.
-            while (it.next(p, total_tiles, sched, cnt, tl)) {
-                const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+        } else {
+            // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
+            TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank, split);
+            Tile ctl;
+            bool c_have = (p.has_c && split == 1) ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
+            int c_chunk = 0;
+            uint32_t c_issued = 0;       // chunks whose C load has been issued
+            auto issue_c = [&](uint32_t chunk_id) {
+                // chunk_id-th chunk of this warp's stream goes to slot chunk_id % kSlots
+                const int nch = (min(BN, p.N - ctl.n0) + 31) / 32;
+                const int sl = static_cast<int>(chunk_id % C::kSlots);
+                const uint32_t dst = slot0 + sl * C::kSlotBytes;
+                const uint32_t bar = cfull_bar(ew, sl);
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, C::kSlotBytes);
+                const int x = ctl.n0 + c_chunk * 32;
+                if (kg) tma_load_3d(dst, &tm_c, bar, x, ctl.d_y + q * 32, ctl.d_z);
+                else tma_load_2d(dst, &tm_c, bar, x, ctl.d_y + q * 32);
+                if (++c_chunk == nch) {
+                    c_chunk = 0;
+                    c_have = cit.next(p, total_tiles, sched, cnt, ctl);
+                }
+            };
+            if (lane == 0) {
+                while (c_have && c_issued + 1 < static_cast<uint32_t>(C::kSlots)) issue_c(c_issued++);
+            }
+
+            uint32_t chunk_id = 0;       // chunks consumed so far
+            if constexpr (kSwiGLU) {
+                // ------------------------------------------ SwiGLU + per-1x128 requantisation
+                // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
+                // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
+                // codes into this warp's slot (32 rows x 128 B, the TMA box) and a byte store of
+                // the scale into its packed word.  Two passes over TMEM: amax, then codes.
+                while (it.next(p, total_tiles, sched, cnt, tl)) {
+                    const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+                    if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
+                    tc_fence_after();
+                    const long long grow = tl.d_row + row;
+                    bool row_ok = row < tl.valid_rows;
+                    if (p.kind == kContiguous) {
+                        const int mi = __ldg(p.m_indices + grow);
+                        if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
+                        row_ok = (mi == tl.g);
+                    }
+                    const int nb = tl.n0 / 256;                      // 128-wide output column block
+                    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+                    float amax = 0.0f;
+                    if (tl.nkb > 0) {
+                        for (int c0 = 0; c0 < 128; c0 += 32) {
+                            uint32_t g[32], u[32];
+                            tmem_ld_32x32b_x32(tacc + c0, g);
+                            tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
+                        }
+                    }
+                    const int e = scale_exponent(amax);
+                    if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
+                    __syncwarp();
+                    uint8_t* rowp = slot0_ptr + lane * 128;
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t g[32], u[32];
+                        if (tl.nkb > 0) {
+                            tmem_ld_32x32b_x32(tacc + c0, g);
+                            tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                            tmem_wait_ld();
+                        } else {
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
+                        }
+                        uint32_t w[8];
+    #pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            uint32_t word = 0;
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
+                            w[k] = word;
+                        }
+                        const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
+                        *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
+                    if (row_ok) {
+                        const int sf_row = p.kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
+                        const int32_t* wp = p.sfq + (p.kind == kMasked ? tl.g * p.sfq_gstride : 0) +
+                                            (long long)(nb >> 2) * p.sfq_ld + sf_row;
+                        *(reinterpret_cast<uint8_t*>(const_cast<int32_t*>(wp)) + (nb & 3)) = static_cast<uint8_t>(e + 127);
+                    }
+                    // Dense rows past M are clipped by the TMA store; grouped layouts store only valid rows.
+                    if (p.kind == kDense || __all_sync(0xffffffffu, row_ok)) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_d, slot0, nb * 128, tl.d_y + q * 32);
+                            bulk_commit_group();
+                        }
+                    } else if (row_ok) {
+                        uint8_t* dst = static_cast<uint8_t*>(p.d) + grow * (p.N / 2) + nb * 128;
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            *reinterpret_cast<uint4*>(dst + 16 * j) = *reinterpret_cast<const uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                    }
+                    __syncwarp();
+                    if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
+                }
+            }
+            while (!kSwiGLU && it.next(p, total_tiles, sched, cnt, tl)) {
+                // warp-uniform decision before the .sync.aligned TMEM loads below
+                const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
                 const long long grow = tl.d_row + row;
@@ -863,222 +949,144 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
                     row_ok = (mi == tl.g);
                 }
-                const int nb = tl.n0 / 256;                      // 128-wide output column block
-                const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-                float amax = 0.0f;
-                if (tl.nkb > 0) {
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t g[32], u[32];
-                        tmem_ld_32x32b_x32(tacc + c0, g);
-                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
-                    }
-                }
-                const int e = scale_exponent(amax);
-                if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
-                __syncwarp();
-                uint8_t* rowp = slot0_ptr + lane * 128;
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t g[32], u[32];
+                // Rows past the end of the D tensor are clipped by the TMA store; the masked and
+                // contiguous layouts have rows inside D that must stay untouched.
+                const bool use_tma = (p.kind == kDense || kg) || __all_sync(0xffffffffu, row_ok);
+                const int ncols = min(BN, p.N - tl.n0);
+                const int nch = (ncols + cw - 1) / cw;
+                for (int ch = 0; ch < nch; ++ch, ++chunk_id) {
+                    const int c0 = ch * cw;
+                    const int sl = static_cast<int>(chunk_id % C::kSlots);
+                    const uint32_t sl_addr = slot0 + sl * C::kSlotBytes;
+                    uint8_t* sl_ptr = slot0_ptr + sl * C::kSlotBytes;
+                    uint32_t r[64];
                     if (tl.nkb > 0) {
-                        tmem_ld_32x32b_x32(tacc + c0, g);
-                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0,
+                                           *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        if (!f32 && c0 + 32 < BN)
+                            tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0 + 32,
+                                               *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                         tmem_wait_ld();
                     } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
+    #pragma unroll
+                        for (int i = 0; i < 64; ++i) r[i] = 0u;
                     }
-                    uint32_t w[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        uint32_t word = 0;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
-                        w[k] = word;
+                    if (!f32 && !(c0 + 32 < BN)) {
+    #pragma unroll
+                        for (int i = 32; i < 64; ++i) r[i] = 0u;
                     }
-                    const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
-                    *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
-                if (row_ok) {
-                    const int sf_row = p.kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
-                    const int32_t* wp = p.sfq + (p.kind == kMasked ? tl.g * p.sfq_gstride : 0) +
-                                        (long long)(nb >> 2) * p.sfq_ld + sf_row;
-                    *(reinterpret_cast<uint8_t*>(const_cast<int32_t*>(wp)) + (nb & 3)) = static_cast<uint8_t>(e + 127);
-                }
-                // Dense rows past M are clipped by the TMA store; grouped layouts store only valid rows.
-                if (p.kind == kDense || __all_sync(0xffffffffu, row_ok)) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tm_d, slot0, nb * 128, tl.d_y + q * 32);
-                        bulk_commit_group();
-                    }
-                } else if (row_ok) {
-                    uint8_t* dst = static_cast<uint8_t*>(p.d) + grow * (p.N / 2) + nb * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(dst + 16 * j) = *reinterpret_cast<const uint4*>(rowp + ((j ^ (lane & 7)) << 4));
-                }
-                __syncwarp();
-                if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
-            }
-        }
-        while (!kSwiGLU && split == 1 && it.next(p, total_tiles, sched, cnt, tl)) {
-            // warp-uniform decision before the .sync.aligned TMEM loads below
-            const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
-            if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-            tc_fence_after();
-            const long long grow = tl.d_row + row;
-            bool row_ok = row < tl.valid_rows;
-            if (p.kind == kContiguous) {
-                const int mi = __ldg(p.m_indices + grow);
-                if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
-                row_ok = (mi == tl.g);
-            }
-            // Rows past the end of the D tensor are clipped by the TMA store; the masked and
-            // contiguous layouts have rows inside D that must stay untouched.
-            const bool use_tma = (p.kind == kDense || kg) || __all_sync(0xffffffffu, row_ok);
-            const int ncols = min(BN, p.N - tl.n0);
-            const int nch = (ncols + cw - 1) / cw;
-            for (int ch = 0; ch < nch; ++ch, ++chunk_id) {
-                const int c0 = ch * cw;
-                const int sl = static_cast<int>(chunk_id % C::kSlots);
-                const uint32_t sl_addr = slot0 + sl * C::kSlotBytes;
-                uint8_t* sl_ptr = slot0_ptr + sl * C::kSlotBytes;
-                uint32_t r[64];
-                if (tl.nkb > 0) {
-                    tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0,
-                                       *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    if (!f32 && c0 + 32 < BN)
-                        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0 + 32,
-                                           *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                    tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) r[i] = 0u;
-                }
-                if (!f32 && !(c0 + 32 < BN)) {
-#pragma unroll
-                    for (int i = 32; i < 64; ++i) r[i] = 0u;
-                }
-                if (ch == nch - 1) {
-                    // the accumulator buffer is free once its last columns are in registers
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (k2Sm && !leader) mbar_arrive_remote(map_shared_rank(acce_bar(acc), 0));
-                        else mbar_arrive(acce_bar(acc));
-                    }
-                }
-                // A 64-column BF16 chunk at the end of a BN = 224 tile would store into the
-                // neighbouring tile: such a chunk takes the per-thread path (no C in BF16).
-                if (use_tma && c0 + cw <= BN) {
-                    if (p.has_c) {
-                        if (lane == 0 && c_issued == chunk_id && c_have) {
-                            // not prefetched (single slot): load now, once the slot's last store is read
-                            bulk_wait_group_read<0>();
-                            issue_c(c_issued++);
-                        }
+                    if (ch == nch - 1) {
+                        // the accumulator buffer is free once its last columns are in registers
+                        tc_fence_before();
                         __syncwarp();
-                        const bool okc = wait_bar(cfull_bar(ew, sl), (chunk_id / C::kSlots) & 1u, wctl, kWaitEpilogueC);
-                        if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
-                    } else {
-                        // the slot's previous store (kSlots chunks ago) must have been read
                         if (lane == 0) {
-                            if (C::kSlots == 1) bulk_wait_group_read<0>();
-                            else bulk_wait_group_read<C::kSlots - 1>();
+                            if (k2Sm && !leader) mbar_arrive_remote(map_shared_rank(acce_bar(acc), 0));
+                            else mbar_arrive(acce_bar(acc));
                         }
+                    }
+                    // A 64-column BF16 chunk at the end of a BN = 224 tile would store into the
+                    // neighbouring tile: such a chunk takes the per-thread path (no C in BF16).
+                    if (use_tma && c0 + cw <= BN) {
+                        if (p.has_c) {
+                            if (lane == 0 && c_issued == chunk_id && c_have) {
+                                // not prefetched (single slot): load now, once the slot's last store is read
+                                bulk_wait_group_read<0>();
+                                issue_c(c_issued++);
+                            }
+                            __syncwarp();
+                            const bool okc = wait_bar(cfull_bar(ew, sl), (chunk_id / C::kSlots) & 1u, wctl, kWaitEpilogueC);
+                            if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
+                        } else {
+                            // the slot's previous store (kSlots chunks ago) must have been read
+                            if (lane == 0) {
+                                if (C::kSlots == 1) bulk_wait_group_read<0>();
+                                else bulk_wait_group_read<C::kSlots - 1>();
+                            }
+                            __syncwarp();
+                        }
+                        uint8_t* rowp = sl_ptr + lane * 128;
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint4* cell = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                            uint4 w;
+                            if (f32) {
+                                float v0 = __uint_as_float(r[4 * j]), v1 = __uint_as_float(r[4 * j + 1]);
+                                float v2 = __uint_as_float(r[4 * j + 2]), v3 = __uint_as_float(r[4 * j + 3]);
+                                if (p.has_c) {
+                                    const float4 cv = *reinterpret_cast<const float4*>(cell);
+                                    v0 += cv.x; v1 += cv.y; v2 += cv.z; v3 += cv.w;
+                                }
+                                w = make_uint4(__float_as_uint(v0), __float_as_uint(v1), __float_as_uint(v2),
+                                               __float_as_uint(v3));
+                            } else {
+                                uint32_t pk[4];
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
+                                                                                    __uint_as_float(r[8 * j + 2 * i + 1]));
+                                    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                w = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                            *cell = w;
+                        }
+                        fence_proxy_async_smem();
                         __syncwarp();
-                    }
-                    uint8_t* rowp = sl_ptr + lane * 128;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4* cell = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
-                        uint4 w;
-                        if (f32) {
-                            float v0 = __uint_as_float(r[4 * j]), v1 = __uint_as_float(r[4 * j + 1]);
-                            float v2 = __uint_as_float(r[4 * j + 2]), v3 = __uint_as_float(r[4 * j + 3]);
-                            if (p.has_c) {
-                                const float4 cv = *reinterpret_cast<const float4*>(cell);
-                                v0 += cv.x; v1 += cv.y; v2 += cv.z; v3 += cv.w;
+                        if (lane == 0) {
+                            if (kg) tma_store_3d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
+                            else tma_store_2d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32);
+                            bulk_commit_group();
+                            if (C::kSlots > 1 && p.has_c && c_have) {
+                                // refill the slot used by the previous chunk, once its store has read it
+                                bulk_wait_group_read<1>();
+                                issue_c(c_issued++);
                             }
-                            w = make_uint4(__float_as_uint(v0), __float_as_uint(v1), __float_as_uint(v2),
-                                           __float_as_uint(v3));
-                        } else {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
-                                                                                __uint_as_float(r[8 * j + 2 * i + 1]));
-                                pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                            }
-                            w = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                         }
-                        *cell = w;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (kg) tma_store_3d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
-                        else tma_store_2d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32);
-                        bulk_commit_group();
-                        if (C::kSlots > 1 && p.has_c && c_have) {
-                            // refill the slot used by the previous chunk, once its store has read it
-                            bulk_wait_group_read<1>();
-                            issue_c(c_issued++);
-                        }
-                    }
-                } else {
-                    // Partially valid row group (no C in these layouts) or a chunk reaching past
-                    // the tile: per-thread stores of the valid rows and columns.  Drain the slot
-                    // stores first so the slot accounting above stays conservative.
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
-                    if (row_ok) {
-                        const int left = ncols - c0;
-                        if (f32) {
-                            float* dp = static_cast<float*>(p.d) + grow * p.N + tl.n0 + c0;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (4 * j < left)
-                                    *reinterpret_cast<uint4*>(dp + 4 * j) =
-                                        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-                        } else {
-                            __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.d) + grow * p.N + tl.n0 + c0;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (8 * j < left) {
-                                    uint32_t pk[4];
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i) {
-                                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                            __uint_as_float(r[8 * j + 2 * i]), __uint_as_float(r[8 * j + 2 * i + 1]));
-                                        pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                    } else {
+                        // Partially valid row group (no C in these layouts) or a chunk reaching past
+                        // the tile: per-thread stores of the valid rows and columns.  Drain the slot
+                        // stores first so the slot accounting above stays conservative.
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+                        if (row_ok) {
+                            const int left = ncols - c0;
+                            if (f32) {
+                                float* dp = static_cast<float*>(p.d) + grow * p.N + tl.n0 + c0;
+    #pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    if (4 * j < left)
+                                        *reinterpret_cast<uint4*>(dp + 4 * j) =
+                                            make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                            } else {
+                                __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.d) + grow * p.N + tl.n0 + c0;
+    #pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    if (8 * j < left) {
+                                        uint32_t pk[4];
+    #pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                                __uint_as_float(r[8 * j + 2 * i]), __uint_as_float(r[8 * j + 2 * i + 1]));
+                                            pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                                        }
+                                        *reinterpret_cast<uint4*>(dp + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                                     }
-                                    *reinterpret_cast<uint4*>(dp + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                                 }
                             }
                         }
                     }
                 }
+                if (aborted) break;
+                if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
-            if (aborted) break;
-            if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
-        }
-        if (lane == 0) {
-            // C loads issued but never consumed (abort) must land before the CTA exits.
-            for (uint32_t c = chunk_id; c < c_issued; ++c)
-                drain_bar(cfull_bar(ew, static_cast<int>(c % C::kSlots)), (c / C::kSlots) & 1u, 20000000ull);
-            bulk_wait_group_read<0>();   // the slots are read; the stores complete with the grid
-        }
-        __syncwarp();
+            if (lane == 0) {
+                // C loads issued but never consumed (abort) must land before the CTA exits.
+                for (uint32_t c = chunk_id; c < c_issued; ++c)
+                    drain_bar(cfull_bar(ew, static_cast<int>(c % C::kSlots)), (c / C::kSlots) & 1u, 20000000ull);
+                bulk_wait_group_read<0>();   // the slots are read; the stores complete with the grid
+            }
+            __syncwarp();
+        }   // not split-K
     }
 
     // ---------------------------------------------------------------- teardown
