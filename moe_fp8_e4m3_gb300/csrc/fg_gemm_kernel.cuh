@@ -177,17 +177,21 @@ struct WaitCtl {
 
 // Bounded mbarrier wait.  Returns false if the CTA is aborting (flag raised here or
 // by another role).
-template <bool kCluster = false>
+// kSleep: a waiting thread sleeps (suspend-time hint) instead of spinning.  Measured on
+// GB300: the GEMM gains (its spinning producer and MMA warps share schedulers with the
+// epilogue), the MQA kernel loses (its epilogue warps wake later) and spins.
+template <bool kCluster = false, bool kSleep = true>
 __device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
-    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    if (kCluster) return mbar_try_wait_cluster(bar, parity);
+    return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity);
 }
 // kCluster: the barrier is also arrived on from the paired CTA (acquire at cluster scope).
-template <bool kCluster = false>
+template <bool kCluster = false, bool kSleep = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, int where) {
-    if (try_wait_scoped<kCluster>(bar, parity)) return true;
+    if (try_wait_scoped<kCluster, kSleep>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (try_wait_scoped<kCluster>(bar, parity)) return true;
+        if (try_wait_scoped<kCluster, kSleep>(bar, parity)) return true;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort = 1;

@@ -123,7 +123,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                 pair_range(p, pr * kTok, lo, hi);
                 if (hi <= lo) continue;
                 if (par == 0) {
-                    if (!wait_bar(qempty_bar(qb), qph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
+                    if (!wait_bar<false, false>(qempty_bar(qb), qph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
                     mbar_arrive_expect_tx(qfull_bar(qb), kTileBytes);
                     tma_load_2d(sbase + kOffQ + qb * kTileBytes, &maps.q, qfull_bar(qb), 0, pr * kTok * kHeads);
                     if (++qb == 2) { qb = 0; qph ^= 1u; }
@@ -132,7 +132,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                     if ((n & 1u) != par) continue;
                     const int s = static_cast<int>(n % kStages);
                     const uint32_t ph = (n / kStages) & 1u;
-                    if (!wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
+                    if (!wait_bar<false, false>(empty_bar(s), ph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
                     mbar_arrive_expect_tx(full_bar(s), kTileBytes);
                     tma_load_2d(sbase + kOffKv + s * kTileBytes, &maps.kv, full_bar(s), 0, t * 128);
                     armed |= 1u << s;
@@ -159,11 +159,11 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                 int lo, hi;
                 pair_range(p, pr * kTok, lo, hi);
                 if (hi <= lo) continue;
-                if (!wait_bar(qfull_bar(qb), qph, wctl, kWaitMma)) { aborted = true; break; }
+                if (!wait_bar<false, false>(qfull_bar(qb), qph, wctl, kWaitMma)) { aborted = true; break; }
                 const uint32_t sq = sbase + kOffQ + qb * kTileBytes;
                 for (int t = lo; t < hi; ++t) {
-                    if (!wait_bar(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
-                    if (!wait_bar(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
+                    if (!wait_bar<false, false>(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
+                    if (!wait_bar<false, false>(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
                     tc_fence_after();
                     const uint32_t skv = sbase + kOffKv + s * kTileBytes;
 #pragma unroll
@@ -230,7 +230,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                 const float sfj = sf_next;
                 const int jn = j + 128;
                 sf_next = (tile + 1 < hi && jn < p.T) ? __ldg(p.kv_sf + jn) : 0.0f;
-                const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+                const bool ok = wait_bar<false, false>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
                 uint32_t v[2][32];
