@@ -12,11 +12,12 @@
 // query token in consecutive TMEM columns, so relu, the head weights and the head sum
 // stay inside the thread; out[i, j..j+31] is then one coalesced store per warp.
 //
-// Warp roles (352 threads): warps 0 and 10 TMA (the pair's q tile once per pair from
+// Warp roles (608 threads): warps 0 and 18 TMA (the pair's q tile once per pair from
 // warp 0; kv tiles through an 8-stage ring, even tiles from warp 0 and odd ones from
-// warp 10: a warp's TMA loads complete one after another, two warps stream in parallel);
-// warp 1 TMEM owner + MMA issuer; warps 2..9 epilogue, one query token of the pair per
-// four warps (warp w reads TMEM lanes 32 (w mod 4) ..).
+// warp 18: a warp's TMA loads complete one after another, two warps stream in parallel);
+// warp 1 TMEM owner + MMA issuer; warps 2..17 epilogue in two sets of eight that take
+// alternate tiles, so two tiles' reductions are in flight; within a set one query token
+// of the pair per four warps (warp w reads TMEM lanes 32 (w mod 4) ..).
 // Three accumulators rotate in TMEM: the hand-off chain epilogue -> MMA -> epilogue is
 // longer than one tile's work.  Every wait is bounded (globaltimer); on
 // expiry the CTA records a time-out in the status word and every role winds down.
@@ -35,7 +36,8 @@ constexpr int kTileBytes = 128 * kDim;                                  // 16 KB
 constexpr int kOffKv = 0;
 constexpr int kOffQ = kOffKv + kStages * kTileBytes;                    // two q buffers
 constexpr int kOffW = kOffQ + 2 * kTileBytes;                           // per epilogue warp: the pair's weights
-constexpr int kEpiWarps = 4 * kTok;
+constexpr int kSetWarps = 4 * kTok;        // epilogue warps of one tile: 4 TMEM lane quarters x 2 tokens
+constexpr int kEpiWarps = 2 * kSetWarps;   // two sets, alternate tiles
 constexpr int kOffSf = kOffW + kEpiWarps * kHeads * 4;                  // unit scale words
 constexpr int kOffBar = kOffSf + 512;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kNumAcc + 1;         // full, empty, qfull, qempty, accf, acce, drain
@@ -85,7 +87,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
         }
         for (int b = 0; b < kNumAcc; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), kEpiWarps);   // one arrive per epilogue warp
+            mbar_init(acce_bar(b), kSetWarps);   // one arrive per epilogue warp of the tile's set
         }
         mbar_init(drain_bar_addr, 1);
         *abort_flag = 0;
@@ -188,15 +190,16 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
         }
         __syncwarp();
     } else {
-        // --------------------------------------------------------------- epilogue (warps 2..9)
+        // --------------------------------------------------------------- epilogue (warps 2..17)
         const int q = warp & 3;                       // TMEM lanes 32q..32q+31
         const int row = q * 32 + lane;
-        const int tok = (warp - 2) / 4;               // the pair's query token this warp reduces
-        const int et = static_cast<int>(threadIdx.x) - 64;   // 0..255 over the epilogue warps
+        const int e = warp - 2;
+        const int tok = (e >> 2) & 1;                 // the pair's query token this warp reduces
+        const unsigned set = static_cast<unsigned>(e >> 3);   // tiles n of this CTA with n % 2 == set
+        const int et = static_cast<int>(threadIdx.x) - 64;   // 0..511 over the epilogue warps
         // each epilogue warp keeps its own copy of its token's head weights (no cross-warp barrier)
-        float* w_s = reinterpret_cast<float*>(smem + kOffW) + (warp - 2) * kHeads;
-        int acc = 0;
-        uint32_t acc_ph = 0;
+        float* w_s = reinterpret_cast<float*>(smem + kOffW) + e * kHeads;
+        unsigned nbase = 0;                           // tiles of this CTA before the current pair
         bool aborted = false;
         for (int pr = blockIdx.x; pr < pairs && !aborted; pr += gridDim.x) {
             const int i0 = pr * kTok;
@@ -224,12 +227,17 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
             const float4* w4 = reinterpret_cast<const float4*>(w_s);
             // kv scales are read one tile ahead: a global load right before the math would
             // put its latency on every tile
-            float sf_next = (lo < hi && lo * 128 + row < p.T) ? __ldg(p.kv_sf + lo * 128 + row) : 0.0f;
-            for (int tile = lo; tile < hi; ++tile) {
+            // this set's first tile of the pair, then every other one
+            const int t0 = lo + static_cast<int>((nbase + set) & 1u);
+            float sf_next = (t0 < hi && t0 * 128 + row < p.T) ? __ldg(p.kv_sf + t0 * 128 + row) : 0.0f;
+            for (int tile = t0; tile < hi; tile += 2) {
+                const unsigned n = nbase + static_cast<unsigned>(tile - lo);
+                const int acc = static_cast<int>(n % kNumAcc);
+                const uint32_t acc_ph = (n / kNumAcc) & 1u;
                 const int j = tile * 128 + row;
                 const float sfj = sf_next;
-                const int jn = j + 128;
-                sf_next = (tile + 1 < hi && jn < p.T) ? __ldg(p.kv_sf + jn) : 0.0f;
+                const int jn = j + 256;
+                sf_next = (tile + 2 < hi && jn < p.T) ? __ldg(p.kv_sf + jn) : 0.0f;
                 const bool ok = wait_bar<false, false>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
@@ -281,8 +289,8 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                     if (j >= ks_i && j < ke_i) p.out[(long long)i * p.T + j] = sum;
                     else if (p.clean) p.out[(long long)i * p.T + j] = -__int_as_float(0x7f800000);
                 }
-                if (++acc == kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
+            if (hi > lo) nbase += static_cast<unsigned>(hi - lo);
         }
     }
     tc_fence_before();
