@@ -723,11 +723,12 @@ int fg_fp8_mqa_logits(int S, int T, int H, int D, const uint8_t* q, const uint8_
     p.pdl = g_pdl;
     fg::MqaMaps mm;
     std::memset(&mm, 0, sizeof(mm));
-    if (!encode_2d(&mm.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 128, (uint64_t)S * 64, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!encode_2d(&mm.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 128, (uint64_t)S * 64, 128, 128, fg::kMqaTokens * 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mm.kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, kv, 128, (uint64_t)T, 128, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return FG_ERR_INVALID_ARG;
-    const int pairs = (S + 1) / 2;
-    const int grid = pairs < sms ? pairs : sms;
+    const int groups = (S + fg::kMqaTokens - 1) / fg::kMqaTokens;
+    const int grid = groups < sms ? groups : sms;
     if (print_configs())
         std::fprintf(stderr, "[fg] fp8_mqa_logits S=%d T=%d H=%d D=%d clean=%d grid=%d\n", S, T, H, D, p.clean, grid);
     if (fg::launch_mqa(p, mm, grid, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {

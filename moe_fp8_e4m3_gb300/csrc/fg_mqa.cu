@@ -6,21 +6,21 @@
 // and -inf elsewhere when clean_logits is set.  Here H = 64 heads and D = 128.
 //
 // The contraction q[i, h, :] . kv[j, :] is an FP8 GEMM with kv tokens on the MMA's M
-// axis (128 per tile) and (query token, head) on N: a tile is 128 kv tokens x 2 query
-// tokens x 64 heads, K = D = 128 (four K=32 MMAs, unit UE8M0 scales).  With kv on M,
-// each epilogue thread owns one kv token j (one TMEM lane) and finds all 64 heads of a
-// query token in consecutive TMEM columns, so relu, the head weights and the head sum
-// stay inside the thread; out[i, j..j+31] is then one coalesced store per warp.
+// axis (128 per tile) and (query token, head) on N: a tile is 128 kv tokens x 4 query
+// tokens x 64 heads (N = 256), K = D = 128 (four K=32 MMAs of kind::f8f6f4: q and kv
+// carry no block scales, the kv scale is applied in the epilogue).  With kv on M, each
+// epilogue thread owns one kv token j (one TMEM lane) and finds all 64 heads of a query
+// token in consecutive TMEM columns, so relu, the head weights and the head sum stay
+// inside the thread; out[i, j..j+31] is then one coalesced store per warp.
 //
-// Warp roles (608 threads): warps 0 and 18 TMA (the pair's q tile once per pair from
-// warp 0; kv tiles through an 8-stage ring, even tiles from warp 0 and odd ones from
-// warp 18: a warp's TMA loads complete one after another, two warps stream in parallel);
-// warp 1 TMEM owner + MMA issuer; warps 2..17 epilogue in two sets of eight that take
-// alternate tiles, so two tiles' reductions are in flight; within a set one query token
-// of the pair per four warps (warp w reads TMEM lanes 32 (w mod 4) ..).
-// Three accumulators rotate in TMEM: the hand-off chain epilogue -> MMA -> epilogue is
-// longer than one tile's work.  Every wait is bounded (globaltimer); on
-// expiry the CTA records a time-out in the status word and every role winds down.
+// Warp roles (576 threads): warp 0 TMA (the group's q tile once per group of four query
+// tokens, kv tiles through an 8-stage ring); warp 1 TMEM owner + MMA issuer; warps 2..17
+// epilogue, one query token of the group per four warps (warp w reads TMEM lanes
+// 32 (w mod 4) ..).
+// Two 256-column accumulators alternate in TMEM.  Four tokens per tile halve the MMA
+// issuer's per-tile work (waits, descriptors, commits) per logit, which bounded the
+// two-token form.  Every wait is bounded (globaltimer); on expiry the CTA records a
+// time-out in the status word and every role winds down.
 #include <cuda_runtime.h>
 
 #include "fg_gemm_kernel.cuh"
@@ -29,25 +29,23 @@
 namespace fg {
 namespace {
 
-constexpr int kHeads = 64, kDim = 128, kTok = 2, kBN = kTok * kHeads;   // N = 128
+constexpr int kHeads = 64, kDim = 128, kTok = kMqaTokens, kBN = kTok * kHeads;   // N = 256
 constexpr int kStages = 8;
-constexpr int kNumAcc = 3;                  // 128-column accumulators in TMEM (+ 8 scale columns)
-constexpr int kTileBytes = 128 * kDim;                                  // 16 KB (kv or q tile)
+constexpr int kNumAcc = 2;                  // 256-column accumulators in TMEM
+constexpr int kKvBytes = 128 * kDim;                                    // 16 KB kv tile
+constexpr int kQBytes = kBN * kDim;                                     // 32 KB q tile
 constexpr int kOffKv = 0;
-constexpr int kOffQ = kOffKv + kStages * kTileBytes;                    // two q buffers
-constexpr int kOffW = kOffQ + 2 * kTileBytes;                           // per epilogue warp: the pair's weights
-constexpr int kSetWarps = 4 * kTok;        // epilogue warps of one tile: 4 TMEM lane quarters x 2 tokens
-constexpr int kEpiWarps = 2 * kSetWarps;   // two sets, alternate tiles
-constexpr int kOffSf = kOffW + kEpiWarps * kHeads * 4;                  // unit scale words
-constexpr int kOffBar = kOffSf + 512;
+constexpr int kOffQ = kOffKv + kStages * kKvBytes;                      // two q buffers
+constexpr int kOffW = kOffQ + 2 * kQBytes;                              // per epilogue warp: its token's weights
+constexpr int kEpiWarps = 4 * kTok;        // 4 TMEM lane quarters x 4 tokens
+constexpr int kOffBar = kOffW + kEpiWarps * kHeads * 4;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 * kNumAcc + 1;         // full, empty, qfull, qempty, accf, acce, drain
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr int kThreads = 64 + 32 * kEpiWarps + 32;   // + a second kv producer warp
-constexpr int kProdWarp2 = kThreads / 32 - 1;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
-// kv tiles [lo, hi) a query-token pair touches; empty when hi <= lo.
-__device__ __forceinline__ void pair_range(const MqaParams& p, int i0, int& lo, int& hi) {
+// kv tiles [lo, hi) a group of query tokens touches; empty when hi <= lo.
+__device__ __forceinline__ void group_range(const MqaParams& p, int i0, int& lo, int& hi) {
     int a = p.T, b = 0;
     for (int t = 0; t < kTok; ++t) {
         const int i = i0 + t;
@@ -57,6 +55,19 @@ __device__ __forceinline__ void pair_range(const MqaParams& p, int i0, int& lo, 
     }
     lo = a / 128;
     hi = b > a ? (b + 127) / 128 : lo;
+}
+
+// Group visited by this CTA in round r: rounds deal the groups to the CTAs in snake order
+// (CTA b takes slot b in even rounds and slot grid-1-b in odd ones), latest query tokens
+// first.  Under causal ranges a group's cost grows with its tokens, so the costly groups
+// go out first and alternate ends of the grid (max per-CTA tiles 127 -> 113 of a mean of
+// 111 at S = T = 4096).  Returns -1 for an empty slot of the last round, kNoGroup past it.
+constexpr int kNoGroup = -2;
+__device__ __forceinline__ int group_of(int r, int groups) {
+    const int c = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    if (r * c >= groups) return kNoGroup;
+    const int slot = r * c + ((r & 1) ? c - 1 - b : b);
+    return slot < groups ? groups - 1 - slot : -1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,7 +98,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
         }
         for (int b = 0; b < kNumAcc; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), kSetWarps);   // one arrive per epilogue warp of the tile's set
+            mbar_init(acce_bar(b), kEpiWarps);   // one arrive per epilogue warp
         }
         mbar_init(drain_bar_addr, 1);
         *abort_flag = 0;
@@ -95,9 +106,6 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
         tma_prefetch_map(&maps.q);
         tma_prefetch_map(&maps.kv);
     }
-    // unit scale factors (UE8M0 127 = 1.0) for the block-scaled MMA
-    if (threadIdx.x < 128) reinterpret_cast<uint32_t*>(smem + kOffSf)[threadIdx.x] = 0x7F7F7F7Fu;
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
@@ -109,34 +117,33 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wctl{abort_flag, p.status, p.timeout_ns};
-    const int pairs = (p.S + kTok - 1) / kTok;
+    const int groups = (p.S + kTok - 1) / kTok;
 
-    if (warp == 0 || warp == kProdWarp2) {
+    if (warp == 0) {
         // ------------------------------------------------------------ TMA producers
         if (lane == 0) {
-            const unsigned par = warp == 0 ? 0u : 1u;    // kv tiles n with n % 2 == par
             int qb = 0;
             uint32_t qph = 0;
             unsigned n = 0;                              // kv tile counter of this CTA
             uint32_t armed = 0, armed_par = 0;
             bool aborted = false;
-            for (int pr = blockIdx.x; pr < pairs && !aborted; pr += gridDim.x) {
+            for (int r = 0, pr; !aborted && (pr = group_of(r, groups)) != kNoGroup; ++r) {
+                if (pr < 0) continue;
                 int lo, hi;
-                pair_range(p, pr * kTok, lo, hi);
+                group_range(p, pr * kTok, lo, hi);
                 if (hi <= lo) continue;
-                if (par == 0) {
+                {
                     if (!wait_bar<false, false>(qempty_bar(qb), qph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
-                    mbar_arrive_expect_tx(qfull_bar(qb), kTileBytes);
-                    tma_load_2d(sbase + kOffQ + qb * kTileBytes, &maps.q, qfull_bar(qb), 0, pr * kTok * kHeads);
+                    mbar_arrive_expect_tx(qfull_bar(qb), kQBytes);
+                    tma_load_2d(sbase + kOffQ + qb * kQBytes, &maps.q, qfull_bar(qb), 0, pr * kTok * kHeads);
                     if (++qb == 2) { qb = 0; qph ^= 1u; }
                 }
                 for (int t = lo; t < hi; ++t, ++n) {
-                    if ((n & 1u) != par) continue;
                     const int s = static_cast<int>(n % kStages);
                     const uint32_t ph = (n / kStages) & 1u;
                     if (!wait_bar<false, false>(empty_bar(s), ph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
-                    mbar_arrive_expect_tx(full_bar(s), kTileBytes);
-                    tma_load_2d(sbase + kOffKv + s * kTileBytes, &maps.kv, full_bar(s), 0, t * 128);
+                    mbar_arrive_expect_tx(full_bar(s), kKvBytes);
+                    tma_load_2d(sbase + kOffKv + s * kKvBytes, &maps.kv, full_bar(s), 0, t * 128);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                 }
@@ -149,36 +156,33 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdesc = make_idesc_mxf8(128, kBN, false, false);
-            const uint32_t sfa_t = tmem_base + kNumAcc * kBN, sfb_t = sfa_t + 4;
-            tc_cp_32x128b_warpx4(sfa_t, make_sdesc(sbase + kOffSf, 0, 128, kLayoutNone));
-            tc_cp_32x128b_warpx4(sfb_t, make_sdesc(sbase + kOffSf, 0, 128, kLayoutNone));
-            const uint32_t idesc = idesc_sf_ids(kIdesc, 0, 0);
+            constexpr uint32_t idesc = make_idesc_f8(128, kBN);
             int s = 0, qb = 0, acc = 0;
             uint32_t ph = 0, qph = 0, acc_ph = 0;
             bool aborted = false;
-            for (int pr = blockIdx.x; pr < pairs && !aborted; pr += gridDim.x) {
+            for (int r = 0, pr; !aborted && (pr = group_of(r, groups)) != kNoGroup; ++r) {
+                if (pr < 0) continue;
                 int lo, hi;
-                pair_range(p, pr * kTok, lo, hi);
+                group_range(p, pr * kTok, lo, hi);
                 if (hi <= lo) continue;
                 if (!wait_bar<false, false>(qfull_bar(qb), qph, wctl, kWaitMma)) { aborted = true; break; }
-                const uint32_t sq = sbase + kOffQ + qb * kTileBytes;
+                const uint32_t sq = sbase + kOffQ + qb * kQBytes;
                 for (int t = lo; t < hi; ++t) {
                     if (!wait_bar<false, false>(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
                     if (!wait_bar<false, false>(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
                     tc_fence_after();
-                    const uint32_t skv = sbase + kOffKv + s * kTileBytes;
+                    const uint32_t skv = sbase + kOffKv + s * kKvBytes;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        tc_mma_mxf8(tmem_base + acc * kBN, make_sdesc(skv + 32 * j, 0, 1024, kLayoutSw128),
-                                    make_sdesc(sq + 32 * j, 0, 1024, kLayoutSw128), idesc, sfa_t, sfb_t, j != 0);
+                        tc_mma_f8(tmem_base + acc * kBN, make_sdesc(skv + 32 * j, 0, 1024, kLayoutSw128),
+                                  make_sdesc(sq + 32 * j, 0, 1024, kLayoutSw128), idesc, j != 0);
                     tc_commit(empty_bar(s));
                     tc_commit(accf_bar(acc));
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                     if (++acc == kNumAcc) { acc = 0; acc_ph ^= 1u; }
                 }
                 if (aborted) break;
-                tc_commit(qempty_bar(qb));      // the pair's q tile is free once its MMAs are done
+                tc_commit(qempty_bar(qb));      // the group's q tile is free once its MMAs are done
                 if (++qb == 2) { qb = 0; qph ^= 1u; }
             }
             // bounded wait until every tensor-core operation issued here has finished
@@ -194,18 +198,19 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
         const int q = warp & 3;                       // TMEM lanes 32q..32q+31
         const int row = q * 32 + lane;
         const int e = warp - 2;
-        const int tok = (e >> 2) & 1;                 // the pair's query token this warp reduces
-        const unsigned set = static_cast<unsigned>(e >> 3);   // tiles n of this CTA with n % 2 == set
+        const int tok = e >> 2;                       // the group's query token this warp reduces
         const int et = static_cast<int>(threadIdx.x) - 64;   // 0..511 over the epilogue warps
         // each epilogue warp keeps its own copy of its token's head weights (no cross-warp barrier)
         float* w_s = reinterpret_cast<float*>(smem + kOffW) + e * kHeads;
-        unsigned nbase = 0;                           // tiles of this CTA before the current pair
+        int acc = 0;
+        uint32_t acc_ph = 0;
         bool aborted = false;
-        for (int pr = blockIdx.x; pr < pairs && !aborted; pr += gridDim.x) {
+        for (int r = 0, pr; !aborted && (pr = group_of(r, groups)) != kNoGroup; ++r) {
+            if (pr < 0) continue;
             const int i0 = pr * kTok;
             const int i = i0 + tok;
             int lo, hi;
-            pair_range(p, i0, lo, hi);
+            group_range(p, i0, lo, hi);
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < kHeads / 32; ++c)
@@ -214,7 +219,7 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
             const int ks_i = i < p.S ? max(__ldg(p.ks + i), 0) : 0;
             const int ke_i = i < p.S ? min(__ldg(p.ke + i), p.T) : 0;
             if (p.clean) {
-                // -inf outside the kv tiles this pair visits
+                // -inf outside the kv tiles this group visits
                 const int c0 = hi > lo ? lo * 128 : p.T, c1 = hi > lo ? min(hi * 128, p.T) : p.T;
                 for (int t = 0; t < kTok; ++t) {
                     const int it = i0 + t;
@@ -227,59 +232,53 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
             const float4* w4 = reinterpret_cast<const float4*>(w_s);
             // kv scales are read one tile ahead: a global load right before the math would
             // put its latency on every tile
-            // this set's first tile of the pair, then every other one
-            const int t0 = lo + static_cast<int>((nbase + set) & 1u);
-            float sf_next = (t0 < hi && t0 * 128 + row < p.T) ? __ldg(p.kv_sf + t0 * 128 + row) : 0.0f;
-            for (int tile = t0; tile < hi; tile += 2) {
-                const unsigned n = nbase + static_cast<unsigned>(tile - lo);
-                const int acc = static_cast<int>(n % kNumAcc);
-                const uint32_t acc_ph = (n / kNumAcc) & 1u;
+            float sf_next = (lo < hi && lo * 128 + row < p.T) ? __ldg(p.kv_sf + lo * 128 + row) : 0.0f;
+            for (int tile = lo; tile < hi; ++tile) {
                 const int j = tile * 128 + row;
                 const float sfj = sf_next;
-                const int jn = j + 256;
-                sf_next = (tile + 2 < hi && jn < p.T) ? __ldg(p.kv_sf + jn) : 0.0f;
+                const int jn = j + 128;
+                sf_next = (tile + 1 < hi && jn < p.T) ? __ldg(p.kv_sf + jn) : 0.0f;
                 const bool ok = wait_bar<false, false>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
-                uint32_t v[2][32];
                 const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + tok * kHeads;
-                tmem_ld_32x32b_x32(ta, v[0]);
-                tmem_ld_32x32b_x32(ta + 32, v[1]);
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce_bar(acc));    // this warp's part is in registers
                 // eight independent partial sums: the head sum is FMA-latency bound as one chain.
                 // For sf[j] > 0, relu(x * sf) = sf * relu(x): the scale is applied once after
-                // the sum; any other scale takes the literal per-head form.
+                // the sum; any other scale takes the literal per-head form.  The 64 heads come
+                // from TMEM in two halves of 32 registers (the block's register budget).
                 float part[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) part[c] = 0.0f;
                 const bool pos = sfj > 0.0f;
-                if (pos) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                        for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 wv = w4[hh * 8 + h4];
-                            float* pc = part + 4 * (h4 & 1);
-                            pc[0] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4]), 0.0f), wv.x, pc[0]);
-                            pc[1] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 1]), 0.0f), wv.y, pc[1]);
-                            pc[2] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 2]), 0.0f), wv.z, pc[2]);
-                            pc[3] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 3]), 0.0f), wv.w, pc[3]);
-                        }
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(ta + 32 * hh, v);
+                    tmem_wait_ld();
+                    if (hh == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acce_bar(acc));    // this warp's part is in registers
                     }
-                } else {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    if (pos) {
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
                             const float4 wv = w4[hh * 8 + h4];
                             float* pc = part + 4 * (h4 & 1);
-                            pc[0] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4]) * sfj, 0.0f), wv.x, pc[0]);
-                            pc[1] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 1]) * sfj, 0.0f), wv.y, pc[1]);
-                            pc[2] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 2]) * sfj, 0.0f), wv.z, pc[2]);
-                            pc[3] = fmaf(fmaxf(__uint_as_float(v[hh][4 * h4 + 3]) * sfj, 0.0f), wv.w, pc[3]);
+                            pc[0] = fmaf(fmaxf(__uint_as_float(v[4 * h4]), 0.0f), wv.x, pc[0]);
+                            pc[1] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), wv.y, pc[1]);
+                            pc[2] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), wv.z, pc[2]);
+                            pc[3] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), wv.w, pc[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 wv = w4[hh * 8 + h4];
+                            float* pc = part + 4 * (h4 & 1);
+                            pc[0] = fmaf(fmaxf(__uint_as_float(v[4 * h4]) * sfj, 0.0f), wv.x, pc[0]);
+                            pc[1] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 1]) * sfj, 0.0f), wv.y, pc[1]);
+                            pc[2] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 2]) * sfj, 0.0f), wv.z, pc[2]);
+                            pc[3] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 3]) * sfj, 0.0f), wv.w, pc[3]);
                         }
                     }
                 }
@@ -289,8 +288,8 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                     if (j >= ks_i && j < ke_i) p.out[(long long)i * p.T + j] = sum;
                     else if (p.clean) p.out[(long long)i * p.T + j] = -__int_as_float(0x7f800000);
                 }
+                if (++acc == kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
-            if (hi > lo) nbase += static_cast<unsigned>(hi - lo);
         }
     }
     tc_fence_before();

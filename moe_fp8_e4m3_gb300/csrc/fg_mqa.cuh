@@ -7,6 +7,9 @@
 
 namespace fg {
 
+// Query tokens per kernel tile: the MMA's N is kMqaTokens x 64 heads.
+constexpr int kMqaTokens = 4;
+
 struct MqaParams {
     int S, T;                 // query tokens, kv tokens
     const float* kv_sf;       // [T]
@@ -21,11 +24,11 @@ struct MqaParams {
 };
 
 struct MqaMaps {
-    CUtensorMap q;            // [S * 64][128] E4M3, boxes of 128 rows (two tokens)
+    CUtensorMap q;            // [S * 64][128] E4M3, boxes of kMqaTokens * 64 rows
     CUtensorMap kv;           // [T][128] E4M3, boxes of 128 rows
 };
 
-// grid CTAs, each walking query-token pairs blockIdx.x, blockIdx.x + grid, ...
+// grid CTAs, each walking groups of kMqaTokens query tokens blockIdx.x, blockIdx.x + grid, ...
 cudaError_t launch_mqa(const MqaParams& p, const MqaMaps& maps, int grid, cudaStream_t stream);
 
 }  // namespace fg

@@ -156,6 +156,16 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_taddr, uint64_t adesc, ui
           "r"(sfb_taddr)
         : "memory");
 }
+// D(tmem) (+)= A(smem) x B(smem)^T, E4M3 inputs without scales, FP32 accumulation in TMEM.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_taddr), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -299,6 +309,12 @@ __host__ __device__ constexpr uint32_t make_idesc_mxf8(int m, int n, bool a_mn_m
                                                        bool b_mn_major) {
     return (a_mn_major ? 1u : 0u) << 15 | (b_mn_major ? 1u : 0u) << 16 |
            static_cast<uint32_t>(n >> 3) << 17 | 1u << 23 | static_cast<uint32_t>(m >> 4) << 24;
+}
+// Instruction descriptor of kind::f8f6f4 without block scaling: FP32 accumulator (D
+// format 1 at bits 4-5), E4M3 x E4M3 (format code 0 at bits 7-9 and 10-12), K-major A and
+// B, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int m, int n) {
+    return 1u << 4 | static_cast<uint32_t>(n >> 3) << 17 | static_cast<uint32_t>(m >> 4) << 24;
 }
 __device__ __forceinline__ uint32_t idesc_sf_ids(uint32_t idesc, uint32_t sfa_id, uint32_t sfb_id) {
     return idesc | (sfb_id & 3u) << 4 | (sfa_id & 3u) << 29;
