@@ -57,6 +57,21 @@ __device__ __forceinline__ void group_range(const MqaParams& p, int i0, int& lo,
     hi = b > a ? (b + 127) / 128 : lo;
 }
 
+// Packed FP32 pairs for fma.rn.f32x2 (x in the low half).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Group visited by this CTA in round r: rounds deal the groups to the CTAs in snake order
 // (CTA b takes slot b in even rounds and slot grid-1-b in odd ones), latest query tokens
 // first.  Under causal ranges a group's cost grows with its tokens, so the costly groups
@@ -246,10 +261,11 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                 // For sf[j] > 0, relu(x * sf) = sf * relu(x): the scale is applied once after
                 // the sum; any other scale takes the literal per-head form.  The 64 heads come
                 // from TMEM in two halves of 32 registers (the block's register budget).
-                float part[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) part[c] = 0.0f;
+                // Partial sums in packed pairs: fma.rn.f32x2 does two of the head products per
+                // instruction (same rounding and the same partial-sum assignment as scalar FMAs).
+                uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
                 const bool pos = sfj > 0.0f;
+                const ulonglong2* w2 = reinterpret_cast<const ulonglong2*>(w4);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t v[32];
@@ -263,25 +279,30 @@ mqa_kernel(const MqaParams p, const __grid_constant__ MqaMaps maps) {
                     if (pos) {
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 wv = w4[hh * 8 + h4];
-                            float* pc = part + 4 * (h4 & 1);
-                            pc[0] = fmaf(fmaxf(__uint_as_float(v[4 * h4]), 0.0f), wv.x, pc[0]);
-                            pc[1] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), wv.y, pc[1]);
-                            pc[2] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), wv.z, pc[2]);
-                            pc[3] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), wv.w, pc[3]);
+                            const ulonglong2 wv = w2[hh * 8 + h4];
+                            uint64_t* pc = part2 + 2 * (h4 & 1);
+                            float r[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) r[c] = fmaxf(__uint_as_float(v[4 * h4 + c]), 0.0f);
+                            pc[0] = ffma2(pack_f32x2(r[0], r[1]), wv.x, pc[0]);
+                            pc[1] = ffma2(pack_f32x2(r[2], r[3]), wv.y, pc[1]);
                         }
                     } else {
 #pragma unroll
                         for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 wv = w4[hh * 8 + h4];
-                            float* pc = part + 4 * (h4 & 1);
-                            pc[0] = fmaf(fmaxf(__uint_as_float(v[4 * h4]) * sfj, 0.0f), wv.x, pc[0]);
-                            pc[1] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 1]) * sfj, 0.0f), wv.y, pc[1]);
-                            pc[2] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 2]) * sfj, 0.0f), wv.z, pc[2]);
-                            pc[3] = fmaf(fmaxf(__uint_as_float(v[4 * h4 + 3]) * sfj, 0.0f), wv.w, pc[3]);
+                            const ulonglong2 wv = w2[hh * 8 + h4];
+                            uint64_t* pc = part2 + 2 * (h4 & 1);
+                            float r[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) r[c] = fmaxf(__uint_as_float(v[4 * h4 + c]) * sfj, 0.0f);
+                            pc[0] = ffma2(pack_f32x2(r[0], r[1]), wv.x, pc[0]);
+                            pc[1] = ffma2(pack_f32x2(r[2], r[3]), wv.y, pc[1]);
                         }
                     }
                 }
+                float part[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) unpack_f32x2(part2[c], part[2 * c], part[2 * c + 1]);
                 const float sum = (((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]))) *
                                   (pos ? sfj : 1.0f);
                 if (i < p.S && j < p.T) {
