@@ -190,8 +190,11 @@ template <bool kCluster = false, bool kSleep = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, int where) {
     if (try_wait_scoped<kCluster, kSleep>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (;;) {
+    for (uint32_t it = 1;; ++it) {
         if (try_wait_scoped<kCluster, kSleep>(bar, parity)) return true;
+        // a spinning wait polls the abort flag and the clock every 32nd round only: each
+        // poll is a shared-memory load competing with the tensor cores' operand reads
+        if (!kSleep && (it & 31u)) continue;
         if (*w.abort) return false;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort = 1;
