@@ -658,7 +658,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
-            uint32_t kcount = 0;
+            uint32_t kcount = 0;    // scale-word copies issued (selects the TMEM scale slot)
             bool aborted = false;
             TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
             Tile tl;
@@ -668,22 +668,29 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 const uint32_t d_t = tmem_base + acc * BN;
                 for (int kb = 0; kb < tl.nkb; ++kb) {
                     if (!wait_bar<k2Sm>(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
-                    fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
                     tc_fence_after();
-                    const uint32_t slot = kcount & 1u;
-                    const uint32_t sfa_t = tmem_base + C::kSfCol0 + slot * 16;
-                    const uint32_t sfb_t = sfa_t + 4;
-                    const uint32_t ssfa = sbase + C::kOffSfa + s * C::kSfaBytes;
-                    const uint32_t ssfb = sbase + C::kOffSfb + s * C::kSfbBytes;
-                    // pair mode: each CTA's scale words go from its shared memory to its TMEM
-                    if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_t, make_sdesc(ssfa, 0, 128, kLayoutNone));
-                    else tc_cp_32x128b_warpx4(sfa_t, make_sdesc(ssfa, 0, 128, kLayoutNone));
-#pragma unroll
-                    for (int i = 0; i < C::kSfbAtoms; ++i) {
-                        if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfb_t + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
-                        else tc_cp_32x128b_warpx4(sfb_t + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
-                    }
+                    // A packed word holds the scales of four consecutive K-groups, so its copy
+                    // to TMEM serves up to four K-groups: copy at the tile's first K-group and
+                    // at every fourth global K-group, alternating between two TMEM slots (the
+                    // copy of the next word never overwrites one still read by MMAs in flight).
                     const uint32_t sf_id = static_cast<uint32_t>(tl.kb0 + kb) & 3u;
+                    if (kb == 0 || sf_id == 0) {
+                        ++kcount;
+                        const uint32_t sfa_n = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                        const uint32_t ssfa = sbase + C::kOffSfa + s * C::kSfaBytes;
+                        const uint32_t ssfb = sbase + C::kOffSfb + s * C::kSfbBytes;
+                        fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
+                        // pair mode: each CTA's scale words go from its shared memory to its TMEM
+                        if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
+                        else tc_cp_32x128b_warpx4(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
+#pragma unroll
+                        for (int i = 0; i < C::kSfbAtoms; ++i) {
+                            if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_n + 4 + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
+                            else tc_cp_32x128b_warpx4(sfa_n + 4 + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
+                        }
+                    }
+                    const uint32_t sfa_t = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                    const uint32_t sfb_t = sfa_t + 4;
                     const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, sf_id);
                     const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
                     const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
@@ -701,7 +708,6 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     }
                     if constexpr (k2Sm) tc_commit_pair_multicast(empty_bar(s));   // frees the stage in both CTAs
                     else tc_commit(empty_bar(s));
-                    ++kcount;
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
                 if (aborted) break;
