@@ -727,8 +727,9 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
         __syncwarp();
     } else if (warp == 2) {
         // ----------------------------------------------------- scale loader
-        // Per stage: the packed UE8M0 word of its K-group for the tile's 128 A rows and BN
-        // B rows, copied with 4-byte cp.async straight into the tcgen05.cp layout (word
+        // Per stage that starts a packed word (the tile's first K-group, then every fourth):
+        // the packed UE8M0 word for the tile's 128 A rows and BN B rows, copied with 4-byte
+        // cp.async straight into the tcgen05.cp layout (word
         // (lane, j) of each 32x4 atom holds MN index j * 32 + lane; rows outside the
         // problem are zero-filled).  Each lane's copies arrive on the stage's full barrier
         // when they land, so this warp never waits for global-load latency.
@@ -777,25 +778,30 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     }
                     __syncwarp();
                 }
-                const int kw = (tl.kb0 + kb) >> 2;
-                const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
-                const uint32_t da = sbase + C::kOffSfa + s * C::kSfaBytes + lane * 16;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int row = tl.sfa_row + lane + 32 * j;
-                    const bool in = row < p.sfa_rows;
-                    cp_async_4(da + 4 * j, in ? pa + row : pa, in ? 4u : 0u);
-                }
-                const int32_t* pb = pb0 + (long long)kw * p.sfb_ld;
-                const uint32_t db = sbase + C::kOffSfb + s * C::kSfbBytes + lane * 16;
-#pragma unroll
-                for (int i = 0; i < C::kSfbAtoms; ++i) {
+                // The MMA issuer copies a packed word to TMEM only at the tile's first K-group
+                // and at every fourth global K-group (one word holds four K-groups' scales):
+                // only those stages need their scale words.
+                if (kb == 0 || ((tl.kb0 + kb) & 3) == 0) {
+                    const int kw = (tl.kb0 + kb) >> 2;
+                    const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
+                    const uint32_t da = sbase + C::kOffSfa + s * C::kSfaBytes + lane * 16;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        int n = tl.n0 + i * 128 + j * 32 + lane;
-                        if constexpr (kSwiGLU) n = swiglu_b_row(p, tl, i) - (tl.b_coord - tl.n0) + j * 32 + lane;
-                        const bool in = n < p.N;
-                        cp_async_4(db + i * 512 + 4 * j, in ? pb + (p.sfb_per_row ? n : (n >> 7)) : pb, in ? 4u : 0u);
+                        const int row = tl.sfa_row + lane + 32 * j;
+                        const bool in = row < p.sfa_rows;
+                        cp_async_4(da + 4 * j, in ? pa + row : pa, in ? 4u : 0u);
+                    }
+                    const int32_t* pb = pb0 + (long long)kw * p.sfb_ld;
+                    const uint32_t db = sbase + C::kOffSfb + s * C::kSfbBytes + lane * 16;
+#pragma unroll
+                    for (int i = 0; i < C::kSfbAtoms; ++i) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            int n = tl.n0 + i * 128 + j * 32 + lane;
+                            if constexpr (kSwiGLU) n = swiglu_b_row(p, tl, i) - (tl.b_coord - tl.n0) + j * 32 + lane;
+                            const bool in = n < p.N;
+                            cp_async_4(db + i * 512 + 4 * j, in ? pb + (p.sfb_per_row ? n : (n >> 7)) : pb, in ? 4u : 0u);
+                        }
                     }
                 }
                 cp_async_mbar_arrive(full_bar(s));
