@@ -1,0 +1,65 @@
+"""Host-side checks of bench.py that need no GPU: the reference arm's JSON line (the CPU
+oracle timed on a bounded sample), the warm-up rule, and the rule that recorded DRAM
+traffic is reported only for the kernel sources it was measured on."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run_bench(*args):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference"
+    assert j["unit"] == "TFLOP/s" and j["higher_is_better"] is True
+    assert j["value"] > 0 and j["steps"] == 1 and j["warmup"] == 3
+    assert "workload" in j["config"]
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_warmup_below_three_is_refused():
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "2")
+    assert r.returncode != 0
+    assert "warmup" in r.stderr
+
+
+def test_recorded_traffic_only_for_current_sources(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+        rec = json.load(fh)
+    workload, kernel = "dense_pair", "prefill"
+    entry = rec[workload][kernel]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["kernel_source_hash"])
+    assert bench.recorded_traffic(workload, kernel) == entry["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic(workload, kernel) is None
+    assert bench.recorded_traffic("no_such_workload", kernel) is None
+
+
+def test_recorded_traffic_matches_the_committed_sources():
+    """The committed ncu traffic was taken on the committed kernel sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+        rec = json.load(fh)
+    hashes = {e["kernel_source_hash"] for wl, ks in rec.items() if not wl.startswith("_")
+              for e in ks.values()}
+    if hashes != {bench.kernel_source_hash()}:
+        pytest.skip("kernel sources changed since the last ncu capture (traffic reported as null)")
+    assert bench.recorded_traffic("prefill", "prefill") is not None
