@@ -17,7 +17,7 @@ Sources, by page and section:
   ``get_tma_aligned_size`` and ``get_mn_major_tma_aligned_packed_ue8m0_tensor``
   (docsearch section 10, README "Utilities").
 
-Readings taken where the pages are silent (each one is also listed in the design doc):
+Readings taken where the pages are silent:
 
 * E4M3 is the OCP FP8 "fn" variant: bias 7, no infinities, S.1111.111 is NaN,
   largest finite 448.

@@ -35,7 +35,7 @@ whether A is stored as [M, K] (N) or [K, M] (T), the second whether B is stored
 transposed, [N, K] (T), or as [K, N] (N).  The scales keep their layouts.  Their oracle
 is the NT definition applied to the operands read in that storage order.
 
-Readings (also listed in the design doc): A scales are 1x128 per row; B scales are one
+Readings where the pages are silent: A scales are 1x128 per row; B scales are one
 per 128x128 block (NT) or 1x128 per column (K-grouped); in the K-grouped layout the
 scale group index is k/128 counted over the concatenated K axis; C is FP32 and only
 present with an FP32 D; BF16 output is round-to-nearest-even of the exact result.
