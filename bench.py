@@ -555,6 +555,22 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------ GPU arm
+def max_over_ranks(torch, dist, value: float, device: str) -> float:
+    """The largest of every rank's `value` (the slowest rank sets a whole-job time);
+    `value` itself on one process."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, step_ms: float) -> float:
+    """Aggregate throughput: every rank does one step of `flops_per_rank_step` in at most
+    `step_ms` (the max over ranks)."""
+    return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
+
+
 def run_gpu(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -621,12 +637,9 @@ def run_gpu(args):
     per_kernel = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
                   for j in range(nl)]                      # ms, mean per launch
     step_ms = sum(steps_ev[i][0].elapsed_time(steps_ev[i][1]) for i in range(args.steps)) / args.steps
-    if dist is not None:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(torch, dist, step_ms, "cuda")
     flops_step = sum(p["flops"] for p in wl.parts)
-    value = world * flops_step / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, step_ms)
 
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs host -> device (pinned), runs the GEMMs and reads the
@@ -666,11 +679,8 @@ def run_gpu(args):
     t_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = t_start.elapsed_time(t_end) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, "cuda")
+    e2e_value = whole_job_tflops(world, flops_step, e2e_ms)
 
     if rank != 0:
         if dist is not None:

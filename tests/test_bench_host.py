@@ -63,3 +63,52 @@ def test_recorded_traffic_matches_the_committed_sources():
     if hashes != {bench.kernel_source_hash()}:
         pytest.skip("kernel sources changed since the last ncu capture (traffic reported as null)")
     assert bench.recorded_traffic("prefill", "prefill") is not None
+
+
+def _gloo_rank(rank, world, port, values, out_q):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(torch, dist, values[rank], "cpu")
+        out_q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    """The N > 1 timing path: every rank ends with the slowest rank's time."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    values = [1.25, 3.5]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gloo_rank, args=(r, 2, port, values, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 3.5, 1: 3.5}
+
+
+def test_whole_job_throughput_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(None, None, 2.0, "cpu") == 2.0
+    # two ranks, 1e12 FLOP each per step, slowest step 2 ms: 1000 TFLOP/s for the job
+    assert bench.whole_job_tflops(2, 1e12, 2.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_prints_only_on_rank_zero():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
