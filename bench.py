@@ -10,20 +10,27 @@ from a seeded torch generator on the GPU, quantised by the library's own quantis
 kernels; L2 is flushed (a write of twice its size) before every timed step, outside
 the timed events.
 
-Two timed passes of --steps steps each:
+Two kinds of timed passes of --steps steps each, each repeated back to back until the
+timed region lasts at least MIN_TIMED_SECONDS (so that the clock sampler sees it):
   1. the step time (the headline value): CUDA events only at the step boundaries, so the
      GEMMs of a step run back to back as a caller issues them (programmatic dependent
      launch lets the second start while the first drains);
   2. the per-kernel durations (the roofline and the per-kernel breakdown): an event
      between consecutive GEMMs, which serialises them.
+The default run then times the other benchmark configurations on the same rules (one
+pass each) and records them in config.kernels: the small dense case (configuration 0,
+launch latency), the M-grouped contiguous (2), masked (3) and K-grouped (4) GEMMs.  Each
+kernel entry gives its fraction of the stated roofs (8 TB/s HBM, 4.5 PFLOP/s dense FP8)
+and of the measured ones (MEASURED_PEAKS.json copy bandwidth; BF16 burst x 2 for FP8).
 
-Other workloads (--workload prefill | decode | contiguous | masked | k_grouped, and the
-other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn, and the fused
-gate-up GEMM contiguous_swiglu, and the indexer's mqa_logits) time the
-single GEMMs on the same rules; they are measurement aids, the default line is the headline.
+Other workloads (--workload prefill | decode | small | contiguous | masked | k_grouped,
+the other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn, the fused
+gate-up GEMM contiguous_swiglu, and the indexer's mqa_logits) time single GEMMs on the
+same rules; they are measurement aids, the default line is the headline.
 
 Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
-CPU oracle instead, on a bounded sample of the same workload.
+CPU oracle instead, on full dense-pair steps (or a bounded sample of each step when
+that many full steps would not end within a few minutes).
 """
 from __future__ import annotations
 
@@ -157,6 +164,7 @@ class DensePair:
     description = ("dense FP8 NT GEMM pair: prefill M=4096 N=7168 K=2048 + decode M=64 N=7168 K=4096; "
                    "A 1x128 / B 128x128 UE8M0 scales; FP32 C accumulated into FP32 D")
     SHAPES = [("prefill", 4096, 7168, 2048), ("decode", 64, 7168, 4096)]
+    WITH_C = True        # FP32 C accumulated into an FP32 D (else no C and a BF16 D)
 
     def __init__(self, torch, fg, seed):
         import workloads
@@ -165,7 +173,7 @@ class DensePair:
         for i, (nm, m, n, k) in enumerate(self.SHAPES):
             xa = workloads.device_normal(seed + 10 * i, (m, k))
             xb = workloads.device_normal(seed + 10 * i + 1, (n, k))
-            c = workloads.device_normal(seed + 10 * i + 2, (m, n))
+            c = workloads.device_normal(seed + 10 * i + 2, (m, n)) if self.WITH_C else None
             a = torch.empty((m, k), dtype=torch.uint8, device="cuda")
             sfa = torch.zeros((cdiv(k, 512), align4(m)), dtype=torch.int32, device="cuda")
             b = torch.empty((n, k), dtype=torch.uint8, device="cuda")
@@ -173,9 +181,10 @@ class DensePair:
             fg.quantize_1x128_rows(xa, a, sfa)
             fg.quantize_128x128_blocks(xb, b, sfb)
             del xa, xb
-            d = torch.empty((m, n), dtype=torch.float32, device="cuda")
+            d = torch.empty((m, n), dtype=torch.float32 if self.WITH_C else torch.bfloat16, device="cuda")
             flops = 2.0 * m * n * k
-            nbytes = m * k + n * k + sfa.numel() * 4 + sfb.numel() * 4 + 2 * m * n * 4
+            nbytes = (m * k + n * k + sfa.numel() * 4 + sfb.numel() * 4 + (m * n * 4 if self.WITH_C else 0)
+                      + m * n * d.element_size())
             self.parts.append({"name": nm, "m": m, "n": n, "k": k, "a": a, "sfa": sfa, "b": b, "sfb": sfb[0],
                                "c": c, "d": d, "flops": flops, "bytes": nbytes})
         torch.cuda.synchronize()
@@ -189,13 +198,19 @@ class DensePair:
         ins, outs = [], []
         for p in self.parts:
             for key in ("a", "sfa", "b", "sfb", "c"):
-                ins.append((p[key], p[key].cpu().pin_memory()))
+                if p[key] is not None:
+                    ins.append((p[key], p[key].cpu().pin_memory()))
             outs.append((p["d"], self.torch.empty_like(p["d"], device="cpu").pin_memory()))
         return ins, outs
 
+    _oracle_inputs = None
+
     @classmethod
     def oracle_inputs(cls):
-        """The same shapes for the CPU oracle: seeded numpy draws quantised by the oracle."""
+        """The same shapes for the CPU oracle: seeded numpy draws quantised by the oracle
+        (made once per process)."""
+        if cls._oracle_inputs is not None:
+            return cls._oracle_inputs
         from oracle import formats as F
         import workloads
         out = []
@@ -204,6 +219,7 @@ class DensePair:
             a, sa = F.quantize_rows(w["a"])
             b, sb = F.quantize_blocks(w["b"])
             out.append({"m": m, "n": n, "k": k, "a": a, "sa": sa, "b": b, "sb": sb, "c": w["c"]})
+        cls._oracle_inputs = out
         return out
 
     @classmethod
@@ -385,6 +401,14 @@ class Decode(DensePair):
     SHAPES = [("decode", 64, 7168, 4096)]
 
 
+class Small(DensePair):
+    """The small dense case: launch latency, not a roofline."""
+    name = "small"
+    description = "dense FP8 NT GEMM M=128 N=256 K=512, no C, BF16 D"
+    SHAPES = [("small", 128, 256, 512)]
+    WITH_C = False
+
+
 class _PrefillLayout(Prefill):
     """The prefill GEMM with its operands stored in another layout (same values, same
     bytes and FLOPs): A as [K, M] for a leading T, B as [K, N] for a trailing N."""
@@ -507,8 +531,16 @@ class ContiguousNN(Contiguous):
                                                                  self.m_indices, self.d)]
 
 
-WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Contiguous, Masked, KGrouped, PrefillNN, PrefillTN,
-                                 PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
+WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, PrefillNN,
+                                 PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
+
+# The benchmark configurations beside the headline pair (recorded in config.kernels of
+# the default run): (configuration number, workload).
+OTHER_CONFIGS = [(0, "small"), (2, "contiguous"), (3, "masked"), (4, "k_grouped")]
+NOMINAL_HBM_GBS = 8000.0        # the stated HBM roof (about 8 TB/s)
+NOMINAL_FP8_TFLOPS = 4500.0     # the stated dense FP8 tensor roof (about 4.5 PFLOP/s)
+MIN_TIMED_SECONDS = 0.5         # repeat the --steps pass until the timed region lasts this long
+REFERENCE_BUDGET_S = 150.0      # CPU seconds the reference arm may spend on its steps
 
 
 # ------------------------------------------------------------------- CPU oracle arm
@@ -525,15 +557,34 @@ def time_oracle(items, min_seconds=10.0, max_reps=8):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle timed on the machine's host cores.  Each step is one
+    full dense-pair step (every output of both GEMMs, the same work as the GPU arm's step
+    and as ``cpu_baseline``) when --warmup + --steps of them fit in REFERENCE_BUDGET_S;
+    otherwise each step is the bounded sample ``oracle_sub_step`` (first rows x columns of
+    each GEMM) so that the run still ends within a few minutes."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     if args.workload != "dense_pair":
         print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the dense_pair workload"}))
         return 0
-    items, sample = DensePair.oracle_sub_step()
     cores = len(os.sched_getaffinity(0))
-    for _ in range(args.warmup):
+    items, sample = DensePair.oracle_full_step()
+    t0 = time.perf_counter()
+    for fn, _f in items:                     # first warm-up step, also the size estimate
+        fn()
+    t_full = time.perf_counter() - t0
+    if (args.warmup - 1 + args.steps) * t_full > REFERENCE_BUDGET_S:
+        # the sample's rows and columns both shrink (the oracle dequantises the columns'
+        # weights on every call), to about `frac` of a full step's work
+        frac = REFERENCE_BUDGET_S / ((args.warmup + args.steps) * t_full)
+        side = math.sqrt(frac)
+        items, sample = DensePair.oracle_sub_step(rows=max(32, int(4096 * side)),
+                                                  cols=max(256, int(7168 * side) // 128 * 128))
+        warm_left = args.warmup
+    else:
+        warm_left = args.warmup - 1
+    for _ in range(warm_left):
         for fn, _f in items:
             fn()
     flops, t0 = 0.0, time.perf_counter()
@@ -571,6 +622,49 @@ def whole_job_tflops(world: int, flops_per_rank_step: float, step_ms: float) -> 
     return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
 
 
+def kernel_entry(p: dict, us: float, peaks: dict) -> dict:
+    """Per-kernel record: time, throughput and its fraction of each roof (the stated
+    nominal roofs first, the measured ones second)."""
+    t = us * 1e-6
+    tflops, gbs = p["flops"] / t / 1e12, p["bytes"] / t / 1e9
+    fp8_measured = peaks["bf16_tflops"] * FP8_OVER_BF16
+    t_roof_nominal = max(p["flops"] / (NOMINAL_FP8_TFLOPS * 1e12), p["bytes"] / (NOMINAL_HBM_GBS * 1e9))
+    t_roof_measured = max(p["flops"] / (fp8_measured * 1e12), p["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    return {
+        "us_per_launch": round(us, 2), "tflops": round(tflops, 1), "hbm_gbs": round(gbs, 1),
+        "algorithmic_bytes": p["bytes"], "flops": p["flops"],
+        "bound": "tensor" if p["flops"] / fp8_measured / 1e12 > p["bytes"] / peaks["hbm_gbs"] / 1e9 else "hbm",
+        "frac_of_roof_nominal": round(t_roof_nominal / t, 3),
+        "frac_of_hbm_nominal": round(gbs / NOMINAL_HBM_GBS, 3),
+        "frac_of_fp8_tensor_nominal": round(tflops / NOMINAL_FP8_TFLOPS, 3),
+        "frac_of_roof": round(t_roof_measured / t, 3),
+        "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3),
+        "frac_of_fp8_tensor": round(tflops / fp8_measured, 3),
+    }
+
+
+def time_steps(torch, launches, steps, flush, stream, per_kernel):
+    """One timed pass of `steps` steps, L2 flushed (outside the events) before each.
+    per_kernel=False: events at the step boundaries only, returns the mean step time (ms).
+    per_kernel=True: an event after every launch, returns the mean time of each (ms)."""
+    nl = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1 if per_kernel else 2)]
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        for j, fn in enumerate(launches):
+            fn()
+            if per_kernel:
+                ev[i][j + 1].record(stream)
+        if not per_kernel:
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if per_kernel:
+        return [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps for j in range(nl)]
+    return sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / steps
+
+
 def run_gpu(args):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -600,32 +694,35 @@ def run_gpu(args):
         flush.fill_(1)
         for fn in launches:
             fn()
+    barrier()
+    # pass length estimate (warm-up steps, flush included) -> passes for the timed region
+    t_est = time.perf_counter()
+    for _ in range(min(args.steps, 20)):
+        flush.fill_(1)
+        for fn in launches:
+            fn()
+    barrier()
+    per_step_s = (time.perf_counter() - t_est) / min(args.steps, 20)
+    passes = max(1, min(200, math.ceil(MIN_TIMED_SECONDS / max(per_step_s * args.steps, 1e-9))))
     st, detail = fg.get_device_error()
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) during warm-up")
 
     nl = len(launches)
-    steps_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     time.sleep(0.3)
     barrier()
     t_wall0 = time.time()
-    # pass 1: step time, events at the step boundaries only
-    for i in range(args.steps):
-        flush.fill_(1)
-        steps_ev[i][0].record(stream)
-        for fn in launches:
-            fn()
-        steps_ev[i][1].record(stream)
+    # pass 1 (x passes): step time, events at the step boundaries only
+    step_runs = []
+    for _ in range(passes):
+        barrier()
+        step_runs.append(time_steps(torch, launches, args.steps, flush, stream, False))
     barrier()
-    # pass 2: per-kernel durations, an event after every GEMM
-    for i in range(args.steps):
-        flush.fill_(1)
-        ev[i][0].record(stream)
-        for j, fn in enumerate(launches):
-            fn()
-            ev[i][j + 1].record(stream)
+    # pass 2 (x passes): per-kernel durations, an event after every GEMM
+    kernel_runs = []
+    for _ in range(passes):
+        kernel_runs.append(time_steps(torch, launches, args.steps, flush, stream, True))
     barrier()
     t_wall1 = time.time()
     time.sleep(0.15)
@@ -634,12 +731,42 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {st} ({detail:#x}) in the timed region")
 
-    per_kernel = [sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)) / args.steps
-                  for j in range(nl)]                      # ms, mean per launch
-    step_ms = sum(steps_ev[i][0].elapsed_time(steps_ev[i][1]) for i in range(args.steps)) / args.steps
+    per_kernel = [sum(r[j] for r in kernel_runs) / passes for j in range(nl)]     # ms, mean per launch
+    step_ms = sum(step_runs) / passes
     step_ms = max_over_ranks(torch, dist, step_ms, "cuda")
     flops_step = sum(p["flops"] for p in wl.parts)
     value = whole_job_tflops(world, flops_step, step_ms)
+    gpu_launches = 2 * nl * args.steps * passes
+
+    # ---- the other benchmark configurations (default run only): each timed alone on the
+    # same rules (L2 flushed before every step, --warmup untimed steps, one pass of --steps)
+    peaks = load_peaks()
+    kernels = {}
+    for j, p in enumerate(wl.parts):
+        kernels[p["name"]] = dict(kernel_entry(p, per_kernel[j] * 1e3, peaks), config=1) \
+            if args.workload == "dense_pair" else kernel_entry(p, per_kernel[j] * 1e3, peaks)
+    if args.workload == "dense_pair" and not args.no_other_configs:
+        for cfg_no, name in OTHER_CONFIGS:
+            owl = WORKLOADS[name](torch, fg, args.seed + 101 * cfg_no + 7919 * rank)
+            ol = owl.launches()
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                for fn in ol:
+                    fn()
+            ot = time_steps(torch, ol, args.steps, flush, stream, True)
+            gpu_launches += len(ol) * args.steps
+            st, detail = fg.get_device_error()
+            if st != 0:
+                raise RuntimeError(f"device status {st} ({detail:#x}) in configuration {cfg_no}")
+            for j, p in enumerate(owl.parts):
+                e = kernel_entry(p, ot[j] * 1e3, peaks)
+                e["config"] = cfg_no
+                e["workload"] = owl.description
+                if cfg_no == 0:
+                    e["note"] = "launch-latency case: report the time, not a roofline fraction"
+                kernels[p["name"]] = e
+            del owl, ol
+            torch.cuda.empty_cache()
 
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs host -> device (pinned), runs the GEMMs and reads the
@@ -687,22 +814,11 @@ def run_gpu(args):
             dist.destroy_process_group()
         return 0
 
-    peaks = load_peaks()
     dom = max(range(nl), key=lambda j: per_kernel[j])
     part = wl.parts[dom]
     achieved = part["bytes"] / (per_kernel[dom] * 1e-3) / 1e9
     traffic = recorded_traffic(wl.name, part["name"])
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    kernels = {}
-    for j, p in enumerate(wl.parts):
-        kernels[p["name"]] = {
-            "us_per_launch": round(per_kernel[j] * 1e3, 2),
-            "tflops": round(p["flops"] / (per_kernel[j] * 1e-3) / 1e12, 1),
-            "hbm_gbs": round(p["bytes"] / (per_kernel[j] * 1e-3) / 1e9, 1),
-            "algorithmic_bytes": p["bytes"], "flops": p["flops"],
-            "frac_of_hbm": round(p["bytes"] / (per_kernel[j] * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
-            "frac_of_fp8_tensor": round(p["flops"] / (per_kernel[j] * 1e-3) / 1e12 / fp8_peak, 3),
-        }
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -710,9 +826,13 @@ def run_gpu(args):
         "data": "synthetic: seeded N(0,1) draws (torch generator on the GPU) quantised by the library's "
                 "UE8M0 quantise kernels",
         "config": {"workload": wl.description, "l2": "flushed before every timed step (write of 2x L2)",
-                   "replicas": world, "pdl": fg.get_pdl(),
-                   "timing": "step: events at step boundaries only; kernels: a second pass with an event "
-                             "after every GEMM",
+                   "replicas": world, "pdl": fg.get_pdl(), "passes": passes,
+                   "timing": f"{passes} back-to-back passes of --steps steps each, averaged; step: events at "
+                             "step boundaries only; kernels: a second set of passes with an event after every "
+                             "GEMM; other configurations: one pass each, an event after every launch",
+                   "roofs": {"nominal": {"hbm_gbs": NOMINAL_HBM_GBS, "fp8_tflops": NOMINAL_FP8_TFLOPS},
+                             "measured": {"hbm_gbs": peaks["hbm_gbs"], "fp8_tflops": round(fp8_peak, 1),
+                                          "source": peaks["source"]}},
                    "kernels": kernels},
         "roofline": ({"bound": "hbm", "kernel": part["name"], "achieved": round(achieved, 1),
                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -734,7 +854,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "overlap": "step i's device-to-host read-back runs beside step i+1's host-to-device copies"},
-        "gpu_launches": 2 * nl * args.steps,
+        "gpu_launches": gpu_launches,
         "cpu_baseline": None,
     }
     if world == 1 and not args.no_cpu_baseline and args.workload == "dense_pair":
@@ -752,12 +872,14 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fg", "reference"], default="fg")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense_pair")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only the headline pair (skip configurations 0, 2, 3 and 4)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -297,10 +297,21 @@ int fg_get_num_sms(void);
 void fg_set_pdl(int enable);
 int fg_get_pdl(void);
 
-/* Synchronises `stream`, then returns and clears the device status word of the
- * current device: FG_OK, FG_ERR_DEVICE_CONTRACT or FG_ERR_DEVICE_TIMEOUT (first event
- * since the last read), or FG_ERR_CUDA if the synchronisation itself failed.
- * *detail (may be NULL) receives the raw code: which check fired and where. */
+/* Reads and clears the device status word of the current device after the work queued
+ * on `stream` so far, then synchronises `stream`: returns FG_OK, FG_ERR_DEVICE_CONTRACT
+ * or FG_ERR_DEVICE_TIMEOUT (the first event since the last read), or FG_ERR_CUDA if a
+ * CUDA call failed.  *detail (may be NULL) receives the raw code:
+ *   0x101  a contiguous m_indices entry names a group >= G
+ *   0x102  a contiguous 128-row block mixes groups (a row names another group than the
+ *          block's first row, or a block whose first row is -1 names a group later on)
+ *   0x103  a masked_m entry lies outside [0, M_max]
+ *   0x104  K-grouped ks entries negative, not multiples of 128, or not summing to K_total
+ *   0x105  internal: a split-K launch without one tile per cluster
+ *   0x2xx  a bounded wait inside a kernel ran out (xx says which role waited)
+ * The word is one per device and shared by every stream: a kernel of another stream that
+ * records an event concurrently is reported by this call or by the next one (the read
+ * and the clear are a single atomic exchange, so no event is lost).  Calls from several
+ * host threads are serialised. */
 int fg_get_device_error(fg_stream_t stream, int* detail);
 
 /* Static description of a status code. */

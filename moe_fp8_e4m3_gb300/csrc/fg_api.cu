@@ -18,6 +18,15 @@
 
 // Device status word: first contract violation or wait time-out since the last read.
 __device__ int g_fg_status = 0;
+// The value taken out of the status word by fg_get_device_error (read back to the host).
+__device__ int g_fg_status_taken = 0;
+
+namespace {
+// Reads and clears the status word in one atomic exchange, in stream order: an event a
+// kernel on another stream records at the same moment lands either in this read or in
+// the word for the next one, never nowhere.
+__global__ void take_status_kernel(int* status, int* taken) { *taken = atomicExch(status, 0); }
+}  // namespace
 
 namespace {
 
@@ -32,12 +41,14 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     int* status = nullptr;
+    int* taken = nullptr;
     // resident clusters of the dense NT kernel per tile width and cluster size 2/4/8
     // (index 3: CTA pairs of the 2-SM kernel); 0 = not queried yet, -1 = query failed
     int clusters[5][4] = {};
 };
 
 std::mutex g_mu;
+std::mutex g_take_mu;   // one status read at a time (they share the device's take slot)
 DeviceState g_dev[kMaxDevices];
 int g_num_sms_limit = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -61,12 +72,15 @@ int device_state(DeviceState** out) {
             return FG_ERR_CUDA;
         }
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_fg_status) != cudaSuccess) {
+        void* ptr_taken = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_fg_status) != cudaSuccess ||
+            cudaGetSymbolAddress(&ptr_taken, g_fg_status_taken) != cudaSuccess) {
             cudaGetLastError();
             return FG_ERR_CUDA;
         }
         st.num_sms = sms;
         st.status = static_cast<int*>(ptr);
+        st.taken = static_cast<int*>(ptr_taken);
         st.ready = true;
     }
     if (!g_encode_tried) {
@@ -826,16 +840,17 @@ int fg_get_device_error(fg_stream_t stream, int* detail) {
     if (detail) *detail = 0;
     DeviceState* st = nullptr;
     if (device_state(&st)) return FG_ERR_CUDA;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-        cudaGetLastError();
-        return FG_ERR_CUDA;
-    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int v = 0;
-    const int zero = 0;
-    if (cudaMemcpy(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
-        cudaGetLastError();
-        return FG_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_take_mu);
+        take_status_kernel<<<1, 1, 0, s>>>(st->status, st->taken);
+        if (cudaGetLastError() != cudaSuccess ||
+            cudaMemcpyAsync(&v, st->taken, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return FG_ERR_CUDA;
+        }
     }
     if (detail) *detail = v;
     if (v == 0) return FG_OK;

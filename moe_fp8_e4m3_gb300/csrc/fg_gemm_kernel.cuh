@@ -213,9 +213,13 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigne
 
 // In CTA-pair mode (dense only) a tile index names a pair of 128-row blocks; `rank`
 // selects this CTA's block and its half of the B rows.
+// scan: the caller is a whole warp walking the tiles together (the scale loader); it
+// checks that a contiguous block whose first row is padding (-1) names no group in any
+// later row (such a block is skipped, so its rows would silently stay unwritten).
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const int* sched,
-                                            const int* cnt, int& cursor, int rank, bool pair, int split) {
+                                            const int* cnt, int& cursor, int rank, bool pair, int split,
+                                            bool scan) {
     Tile tl;
     tl.skip = false;
     tl.g = 0;
@@ -242,6 +246,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
         const int mb = t / p.num_nb, nb = t % p.num_nb;
         const int g = __ldg(p.m_indices + (long long)mb * 128);
         tl.n0 = nb * BN;
+        if (scan && g < 0) {
+            const int lane = threadIdx.x & 31;
+            const int32_t* blk = p.m_indices + (long long)mb * 128;
+            bool named = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) named |= __ldg(blk + lane + 32 * j) >= 0;
+            if (__any_sync(0xffffffffu, named) && lane == 0) record_status(p.status, kErrContract | kChkMixedBlock);
+        }
         if (g < 0 || g >= p.G) {
             if (g >= p.G) record_status(p.status, kErrContract | kChkGroupIndex);
             tl.skip = true;
@@ -297,9 +309,9 @@ struct TileIter {
     bool pair;
     int split;
     __device__ __forceinline__ bool next(const GemmParams& p, int total, const int* sched, const int* cnt,
-                                         Tile& tl) {
+                                         Tile& tl, bool scan = false) {
         while (t < total) {
-            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair, split);
+            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair, split, scan);
             t += stride;
             if (!tl.skip) return true;
         }
@@ -742,7 +754,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
         TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
         Tile tl;
         bool aborted = false;
-        while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
+        while (!aborted && it.next(p, total_tiles, sched, cnt, tl, p.kind == kContiguous)) {
             const int32_t* pa0 = p.sfa + tl.sfa_g * p.sfa_gstride;
             const int32_t* pb0 = p.sfb + tl.g * p.sfb_gstride;
             for (int kb = 0; kb < tl.nkb; ++kb) {

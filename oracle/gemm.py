@@ -152,24 +152,28 @@ def m_grouped_fp8_gemm_nn_contiguous(a, sfa_words, b, sfb_words, m_indices, rows
 # ---------------------------------------------------------------------------
 # M-grouped masked
 # ---------------------------------------------------------------------------
-def m_grouped_fp8_gemm_nt_masked(a, sfa_words, b, sfb_words, masked_m, experts=None):
+def m_grouped_fp8_gemm_nt_masked(a, sfa_words, b, sfb_words, masked_m, experts=None, rows=None):
     """a: uint8 [G, M_max, K]; sfa_words: int32 [G][ceil(K/512)][align4(M_max)];
     b: uint8 [G, N, K]; sfb_words: int32 [G][ceil(K/512)][align4(ceil(N/128))];
     masked_m: int [G].
 
     Returns {g: float64 [masked_m[g], N]} for the selected experts: only rows
-    m < masked_m[g] are computed; every other row of D is left as it was."""
+    m < masked_m[g] are computed; every other row of D is left as it was.
+    ``rows`` (optional, {g: row indices}) restricts expert g's output to those rows, each
+    below masked_m[g], in the order given."""
     g_count, m_max, k = a.shape
     n = b.shape[1]
     out = {}
     for e in (range(g_count) if experts is None else experts):
         valid = int(masked_m[e])
-        if valid <= 0:
+        sel = np.arange(max(valid, 0)) if rows is None else np.asarray(rows[e], dtype=np.int64)
+        assert np.all(sel < valid), "rows beyond the mask are not computed"
+        if len(sel) == 0:
             out[e] = np.zeros((0, n))
             continue
-        sa = row_scales(sfa_words[e], m_max, k)[:valid]
+        sa = row_scales(sfa_words[e], m_max, k)[sel]
         be = dequant_k_major(b[e], block_scales(sfb_words[e], n, k))
-        out[e] = dequant_k_major(a[e, :valid], sa) @ be.T
+        out[e] = dequant_k_major(a[e, sel], sa) @ be.T
     return out
 
 

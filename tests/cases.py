@@ -100,9 +100,9 @@ def masked_case(seed, **kw):
             "sfb": np.stack(sfb), "masked_m": w["masked_m"]}
 
 
-def masked_ref(case, experts=None):
+def masked_ref(case, experts=None, rows=None):
     return oracle.m_grouped_fp8_gemm_nt_masked(case["a"], case["sfa"], case["b"], case["sfb"],
-                                               case["masked_m"], experts=experts)
+                                               case["masked_m"], experts=experts, rows=rows)
 
 
 # -------------------------------------------------------------- K-grouped

@@ -112,3 +112,20 @@ def test_reference_arm_prints_only_on_rank_zero():
                         "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_reference_arm_samples_each_step_when_full_steps_do_not_fit(monkeypatch, capsys):
+    """With many steps the reference arm bounds its work: each step becomes the first rows
+    of every output (the sample is named in the line)."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "REFERENCE_BUDGET_S", 0.05)
+    # smaller shapes of the same pair keep the CPU suite quick
+    monkeypatch.setattr(bench.DensePair, "SHAPES", [("prefill", 512, 1024, 512), ("decode", 64, 1024, 1024)])
+    monkeypatch.setattr(bench.DensePair, "_oracle_inputs", None)
+    args = argparse.Namespace(workload="dense_pair", steps=50, warmup=3, gpus=1)
+    assert bench.run_reference(args) == 0
+    j = json.loads([ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")][0])
+    assert j["steps"] == 50 and j["value"] > 0
+    assert "first" in j["cpu_baseline"]["sample"]

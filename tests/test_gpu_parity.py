@@ -197,6 +197,33 @@ def test_contiguous_contract_violation_reported(fg):
     assert np.all(d.is_sentinel()[128:]) and not np.any(d.is_sentinel()[:128])
 
 
+def test_contiguous_padding_first_block_naming_a_group_reported(fg):
+    """A block whose first row is padding (-1) is skipped; if a later row of it names a
+    group the layout is malformed (segments must start on 128-row boundaries): the call
+    reports it (0x102) and leaves the whole block untouched."""
+    from gpu_util import GuardedOut, dev
+    g = np.random.Generator(np.random.PCG64(33))
+    m_indices = np.array([0] * 128 + [-1] * 5 + [1] * 123 + [1] * 128, np.int32)
+    k, n = 256, 128
+    a = P.rand_codes(g, (len(m_indices), k))
+    b = P.rand_codes(g, (2, n, k))
+    sfa = P.rand_words(g, len(m_indices), k // 128)
+    sfb = np.stack([P.rand_words(g, 1, k // 128) for _ in range(2)])
+    d = GuardedOut(len(m_indices), n, "bf16")
+    fg.m_grouped_fp8_gemm_nt_contiguous(dev(a), dev(sfa), dev(b), dev(sfb), dev(m_indices), d.tensor)
+    st, detail = fg.get_device_error()
+    assert st == fg.FG_ERR_DEVICE_CONTRACT and detail == 0x102, (st, hex(detail))
+    d.check_guards()
+    sent = d.is_sentinel()
+    assert np.all(sent[128:256]) and not np.any(sent[:128]) and not np.any(sent[256:])
+    case = {"m_total": len(m_indices), "n": n, "k": k, "g": 2, "a": a, "sfa": sfa, "b": b, "sfb": sfb,
+            "m_indices": m_indices}
+    ref, _ = C.contiguous_ref(case)
+    vals = d.values()
+    C.compare(vals[:128], ref[:128], "block 0")
+    C.compare(vals[256:], ref[256:], "block 2")
+
+
 # ----------------------------------------------------------------- masked
 def run_masked(fg, case, out="bf16"):
     from gpu_util import GuardedOut, dev
@@ -223,6 +250,16 @@ def _check_masked(case, d):
 def test_masked_parity(fg, masks):
     case = C.masked_case(3, num_groups=4, m_max=192, n=256, k=384, masked_m=masks)
     _check_masked(case, run_masked(fg, case))
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_masked_m_max_not_multiple_of_32(fg, out):
+    """M_max = 200: the second 128-row block of a group reaches into the next group's rows
+    (or past the end of A for the last group); only rows below the mask are written, and
+    masks cover 0, 1, 31, 32, 127, 128, 129, 199 and 200 rows."""
+    masks = [0, 1, 31, 32, 127, 128, 129, 199, 200]
+    case = C.masked_case(8, num_groups=len(masks), m_max=200, n=272, k=384, masked_m=masks)
+    _check_masked(case, run_masked(fg, case, out))
 
 
 def test_masked_random_masks(fg):

@@ -3,6 +3,8 @@
 of tests/golden/closed_forms.json, and segment logic.  The mutation test plants
 plausible mistakes in a copy of the oracle (on the CPU) and checks that the pins
 catch every one of them."""
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -218,3 +220,61 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
         except Exception:  # noqa: BLE001 - any failure counts as caught
             caught.append(check.__name__)
     assert caught, f"no pin detects mutant {name}"
+
+
+def _exact_and_magnitude(terms_a, terms_b):
+    """Exact sum of the products and the sum of their magnitudes."""
+    tot, mag = Fraction(0), Fraction(0)
+    for x, y in zip(terms_a, terms_b):
+        p = x * y
+        tot += p
+        mag += abs(p)
+    return tot, mag
+
+
+def test_oracle_long_k_wide_range_exact():
+    """The accumulation case of the FP8 GEMM (article "Deepseek AI Libera DeepGEMM",
+    "Details and technical benefits": fine-grained scales with FP32 promotion so that long
+    accumulations stay accurate): at K = 16384 with per-group magnitudes spanning about
+    +-20 binades, the oracle's FP64 result agrees with an exact rational sum over every
+    term to FP64 rounding of the sum of magnitudes."""
+    import workloads
+    m, n, k = 3, 130, 16384
+    w = workloads.dense_wide_range(77, m, n, k, True)
+    a, sa = F.quantize_rows(w["a"])
+    b, sb = F.quantize_blocks(w["b"])
+    sfa, sfb = F.pack_ue8m0(sa), F.pack_ue8m0(sb)
+    got = oracle.fp8_gemm_nt(a, sfa, b, sfb, w["c"])
+    # the scales really span the intended range (bytes 127 +- about 10 each)
+    assert int(sa.max()) - int(sa.min()) >= 18 and int(sb.max()) - int(sb.min()) >= 18
+    for (i, j) in [(0, 0), (1, 129), (2, 64)]:
+        ta = [P.fr_e4m3(a[i, kk]) * P.fr_ue8(P.word_byte(sfa, kk // 128, i)) for kk in range(k)]
+        tb = [P.fr_e4m3(b[j, kk]) * P.fr_ue8(P.word_byte(sfb, kk // 128, j // 128)) for kk in range(k)]
+        tot, mag = _exact_and_magnitude(ta, tb)
+        tot += Fraction(float(w["c"][i, j]))
+        assert P.close_fp64(float(got[i, j]), tot, mag + 1, k), (i, j)
+        # the falling magnitudes: the last quarter of K contributes far less than the first
+        q = k // 4
+        first, _ = _exact_and_magnitude(ta[:q], tb[:q])
+        _, last_mag = _exact_and_magnitude(ta[-q:], tb[-q:])
+        assert last_mag < Fraction(1, 2 ** 10) * max(abs(first), Fraction(1, 2 ** 20))
+
+
+def test_oracle_k_grouped_single_long_segment_exact():
+    """One expert owns the whole K axis (ks = [16384, 0, 0]): its output is the exact
+    rational sum; the empty experts' outputs are C."""
+    import workloads
+    m, n = 2, 3
+    w = workloads.k_grouped_wide_range(78, [16384, 0, 0], m, n)
+    a, sa = F.quantize_cols(w["a"])
+    b, sb = F.quantize_cols(w["b"])
+    sfa, sfb = F.pack_ue8m0(sa), F.pack_ue8m0(sb)
+    out = oracle.k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, w["ks"], w["c"])
+    for (i, j) in [(0, 0), (1, 2)]:
+        exact = P.exact_k_grouped(a, sfa, b, sfb, w["ks"], w["c"], 0, i, j)
+        ta = [P.fr_e4m3(a[kk, i]) * P.fr_ue8(P.word_byte(sfa, kk // 128, i)) for kk in range(16384)]
+        tb = [P.fr_e4m3(b[kk, j]) * P.fr_ue8(P.word_byte(sfb, kk // 128, j)) for kk in range(16384)]
+        _, mag = _exact_and_magnitude(ta, tb)
+        assert P.close_fp64(float(out[0][i, j]), exact, mag + 1, 16384), (i, j)
+    for e in (1, 2):
+        assert np.array_equal(out[e], w["c"][e].astype(np.float64))

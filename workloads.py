@@ -51,6 +51,46 @@ def dense(seed: int, m: int, n: int, k: int, with_c: bool) -> dict:
     return out
 
 
+def falling_sigmas(g: np.random.Generator, rows: int, groups: int, spread: int) -> np.ndarray:
+    """Standard deviations 2^e for `rows` x `groups` blocks, e falling from +spread at the
+    first 128-wide K-group to -spread at the last (linear trend), plus an integer jitter in
+    [-2, 2] per block, clipped to [-spread, spread]."""
+    trend = np.rint(spread * (1.0 - 2.0 * np.arange(groups) / max(groups - 1, 1)))
+    e = np.clip(trend[None, :] + g.integers(-2, 3, (rows, groups)), -spread, spread)
+    return np.exp2(e).astype(np.float32)
+
+
+def dense_wide_range(seed: int, m: int, n: int, k: int, with_c: bool, spread: int = 10) -> dict:
+    """Dense draws whose magnitude changes from one 128-wide K-group to the next: element
+    (i, k) of A ~ N(0, s_a[i, k/128]^2) with s_a from ``falling_sigmas`` per row, element
+    (j, k) of B ~ N(0, s_b[j/128, k/128]^2) per 128-row block; C ~ N(0, 1).  Products of
+    the two span about 2 * spread binades either side of 1, largest in the first K-groups,
+    so the smallest groups are accumulated last."""
+    g = rng(seed)
+    groups = k // ALIGN
+    sa = np.repeat(falling_sigmas(g, m, groups, spread), ALIGN, axis=1)
+    sb = np.repeat(np.repeat(falling_sigmas(g, (n + ALIGN - 1) // ALIGN, groups, spread), ALIGN, axis=0)[:n],
+                   ALIGN, axis=1)
+    out = {"a": _normal(g, (m, k)) * sa, "b": _normal(g, (n, k)) * sb, "c": None}
+    if with_c:
+        out["c"] = _normal(g, (m, n))
+    return out
+
+
+def k_grouped_wide_range(seed: int, ks, m: int, n: int, spread: int = 10) -> dict:
+    """K-grouped draws (segments ``ks``, multiples of 128, no padding rows) with the
+    magnitudes of ``dense_wide_range`` along the concatenated K axis: element (k, i) of A ~
+    N(0, s_a[i, k/128]^2) per column i of A, likewise for B; C[G, M, N] ~ N(0, 1)."""
+    g = rng(seed)
+    ks = np.asarray(ks, dtype=np.int64)
+    k_total = int(ks.sum())
+    groups = k_total // ALIGN
+    sa = np.repeat(falling_sigmas(g, m, groups, spread), ALIGN, axis=1).T
+    sb = np.repeat(falling_sigmas(g, n, groups, spread), ALIGN, axis=1).T
+    return {"a": _normal(g, (k_total, m)) * sa, "b": _normal(g, (k_total, n)) * sb,
+            "ks": ks.astype(np.int32), "c": _normal(g, (len(ks), m, n))}
+
+
 def routing(g: np.random.Generator, num_tokens: int, num_routed: int, topk: int, num_groups: int):
     """Uniform random logits, top-k experts per token; the rows routed to experts
     0..num_groups-1 grouped by expert (ascending token order), each segment padded to a
