@@ -7,8 +7,11 @@ Default workload (the headline metric's configuration): the dense FP8 NT GEMM pa
 with A scaled per 1x128 row group, B per 128x128 block (UE8M0), and an FP32 C
 accumulated into an FP32 D.  One step = one call of each.  Inputs are N(0,1) draws
 from a seeded torch generator on the GPU, quantised by the library's own quantise
-kernels; L2 is flushed (a write of twice its size) before every timed step, outside
-the timed events.
+kernels.  L2 rule (--l2 auto): a workload whose step moves more than twice the L2 size
+(the dense pair: 291 MB against 129 MB; the grouped configurations too) runs back to back
+without a flush, since nothing of one step survives in L2 to the next; a smaller one (the
+128x256x512 case) has L2 flushed before every timed step (a write of twice its size),
+outside the timed events.  --l2 flush forces the flush everywhere.
 
 Two kinds of timed passes of --steps steps each, each repeated back to back until the
 timed region lasts at least MIN_TIMED_SECONDS (so that the clock sampler sees it):
@@ -345,7 +348,8 @@ class Masked:
 class KGrouped:
     name = "k_grouped"
     description = ("K-grouped contiguous FP8 TN GEMM: 8 experts, M=4096 N=2048, K segments ~ Multinomial(16384) "
-                   "padded to 128, 1x128 scales along K, FP32 C accumulated into FP32 D")
+                   "padded to 128, 1x128 scales along K, results accumulated into the FP32 C [8,4096,2048] in place "
+                   "(D is C)")
 
     def __init__(self, torch, fg, seed):
         import numpy as np
@@ -372,7 +376,7 @@ class KGrouped:
         del xa, xb
         self.ks = torch.from_numpy(ks.astype(np.int32)).cuda()
         self.c = workloads.device_normal(seed + 60, (g, m, n))
-        self.d = torch.empty((g, m, n), dtype=torch.float32, device="cuda")
+        self.d = self.c            # the weight gradient accumulates into C itself
         self.flops = 2.0 * m * n * float(ks_true.sum())
         self.bytes = k_total * (m + n) + self.sfa.numel() * 4 + self.sfb.numel() * 4 + 2 * g * m * n * 4
         self.parts = [{"name": "k_grouped", "flops": self.flops, "bytes": self.bytes}]
@@ -385,6 +389,18 @@ class KGrouped:
     def e2e_io(self):
         ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.ks, self.c)]
         return ins, [(self.d, self.torch.empty_like(self.d, device="cpu").pin_memory())]
+
+
+class KGroupedSeparate(KGrouped):
+    """The K-grouped workload with a separate D (C read, D written): measurement aid."""
+    name = "k_grouped_separate_d"
+    description = KGrouped.description.replace("results accumulated into the FP32 C [8,4096,2048] in place (D is C)",
+                                               "FP32 C [8,4096,2048] added into a separate FP32 D")
+
+    def __init__(self, torch, fg, seed):
+        super().__init__(torch, fg, seed)
+        self.d = torch.empty_like(self.c)
+        torch.cuda.synchronize()
 
 
 class Prefill(DensePair):
@@ -531,7 +547,7 @@ class ContiguousNN(Contiguous):
                                                                  self.m_indices, self.d)]
 
 
-WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, PrefillNN,
+WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, PrefillNN,
                                  PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
 
 # The benchmark configurations beside the headline pair (recorded in config.kernels of
@@ -644,14 +660,16 @@ def kernel_entry(p: dict, us: float, peaks: dict) -> dict:
 
 
 def time_steps(torch, launches, steps, flush, stream, per_kernel):
-    """One timed pass of `steps` steps, L2 flushed (outside the events) before each.
+    """One timed pass of `steps` steps, L2 flushed (outside the events) before each when
+    `flush` is a buffer (None: no flush).
     per_kernel=False: events at the step boundaries only, returns the mean step time (ms).
     per_kernel=True: an event after every launch, returns the mean time of each (ms)."""
     nl = len(launches)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1 if per_kernel else 2)]
           for _ in range(steps)]
     for i in range(steps):
-        flush.fill_(1)
+        if flush is not None:
+            flush.fill_(1)
         ev[i][0].record(stream)
         for j, fn in enumerate(launches):
             fn()
@@ -682,7 +700,18 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+
+    def flush_for(work):
+        """The L2 rule of a workload: flush before every step (a write of 2x L2) unless one
+        step reads and writes more than twice the L2 size by itself."""
+        step_bytes = sum(p["bytes"] for p in work.parts)
+        if args.l2 == "flush" or (args.l2 == "auto" and step_bytes < 2 * l2):
+            return flush_buf, "flushed before every timed step (write of 2x L2)"
+        return None, (f"not flushed: one step moves {step_bytes / 1e6:.0f} MB, more than twice the "
+                      f"{l2 / 1e6:.0f} MB L2")
+
+    flush, l2_note = flush_for(wl)
 
     def barrier():
         torch.cuda.synchronize()
@@ -691,14 +720,16 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        if flush is not None:
+            flush.fill_(1)
         for fn in launches:
             fn()
     barrier()
     # pass length estimate (warm-up steps, flush included) -> passes for the timed region
     t_est = time.perf_counter()
     for _ in range(min(args.steps, 20)):
-        flush.fill_(1)
+        if flush is not None:
+            flush.fill_(1)
         for fn in launches:
             fn()
     barrier()
@@ -739,7 +770,7 @@ def run_gpu(args):
     gpu_launches = 2 * nl * args.steps * passes
 
     # ---- the other benchmark configurations (default run only): each timed alone on the
-    # same rules (L2 flushed before every step, --warmup untimed steps, one pass of --steps)
+    # same rules (the L2 rule above, --warmup untimed steps, one pass of --steps)
     peaks = load_peaks()
     kernels = {}
     for j, p in enumerate(wl.parts):
@@ -749,11 +780,13 @@ def run_gpu(args):
         for cfg_no, name in OTHER_CONFIGS:
             owl = WORKLOADS[name](torch, fg, args.seed + 101 * cfg_no + 7919 * rank)
             ol = owl.launches()
+            oflush, onote = flush_for(owl)
             for _ in range(args.warmup):
-                flush.fill_(1)
+                if oflush is not None:
+                    oflush.fill_(1)
                 for fn in ol:
                     fn()
-            ot = time_steps(torch, ol, args.steps, flush, stream, True)
+            ot = time_steps(torch, ol, args.steps, oflush, stream, True)
             gpu_launches += len(ol) * args.steps
             st, detail = fg.get_device_error()
             if st != 0:
@@ -762,6 +795,7 @@ def run_gpu(args):
                 e = kernel_entry(p, ot[j] * 1e3, peaks)
                 e["config"] = cfg_no
                 e["workload"] = owl.description
+                e["l2"] = onote
                 if cfg_no == 0:
                     e["note"] = "launch-latency case: report the time, not a roofline fraction"
                 kernels[p["name"]] = e
@@ -825,7 +859,7 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
         "data": "synthetic: seeded N(0,1) draws (torch generator on the GPU) quantised by the library's "
                 "UE8M0 quantise kernels",
-        "config": {"workload": wl.description, "l2": "flushed before every timed step (write of 2x L2)",
+        "config": {"workload": wl.description, "l2": l2_note,
                    "replicas": world, "pdl": fg.get_pdl(), "passes": passes,
                    "timing": f"{passes} back-to-back passes of --steps steps each, averaged; step: events at "
                              "step boundaries only; kernels: a second set of passes with an event after every "
@@ -878,6 +912,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense_pair")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
+                    help="auto: flush L2 before every step unless one step moves more than twice L2")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="time only the headline pair (skip configurations 0, 2, 3 and 4)")
     args = ap.parse_args()

@@ -26,7 +26,10 @@
  *   - A scales are one per row per K-group (1x128).  B scales of the NT calls are
  *     one per 128x128 block (MN index = n / 128); the K-grouped call takes 1x128
  *     scales along K for both operands.
- *   - C is optional FP32 and is accepted only with an FP32 D; D may alias C.
+ *   - C is optional FP32 and is accepted only with an FP32 D.  D may alias C (the same
+ *     pointer: in-place accumulation, D += A @ B^T; the kernels then read no C of their own
+ *     and add the product onto D with TMA reduce-adds, one FP32 add per element performed
+ *     in L2).  C and D that overlap without being the same array are not supported.
  *     A BF16 D is round-to-nearest-even of the FP32 accumulator.
  *   - Alignment: A, B, C, D and the scale arrays must be 16-byte aligned;
  *     index arrays 4-byte aligned.  K (or every K segment) is a multiple of 128,
@@ -45,8 +48,8 @@
  *   - Environment switches (tuning and diagnosis aids; the defaults are the measured
  *     best): FG_FORCE_BN=64|128|192|224|256 forces the N tile where that width applies;
  *     FG_FORCE_SPLIT=1|2|4|8 forces the dense split-K cluster size (a split that cannot
- *     run falls back to the cost model); FG_2SM=1 selects the CTA-pair (2-SM MMA) dense
- *     kernel; FG_PRINT_CONFIGS=1 prints each launch's tiling to stderr.  Only a split
+ *     run falls back to the cost model); FG_PRINT_CONFIGS=1 prints each launch's tiling to
+ *     stderr.  Only a split
  *     changes the FP32 summation order; every choice stays within the stated tolerance.
  */
 #ifndef FG_H

@@ -42,9 +42,9 @@ struct DeviceState {
     int num_sms = 0;
     int* status = nullptr;
     int* taken = nullptr;
-    // resident clusters of the dense NT kernel per tile width and cluster size 2/4/8
-    // (index 3: CTA pairs of the 2-SM kernel); 0 = not queried yet, -1 = query failed
-    int clusters[5][4] = {};
+    // resident split-K clusters of the dense NT kernel per tile width and cluster size
+    // 2/4/8; 0 = not queried yet, -1 = query failed
+    int clusters[5][3] = {};
 };
 
 std::mutex g_mu;
@@ -102,32 +102,23 @@ int sms_in_use(const DeviceState& st) {
     return (g_num_sms_limit > 0 && g_num_sms_limit < st.num_sms) ? g_num_sms_limit : st.num_sms;
 }
 
-// Clusters of `cluster` CTAs (2, 4 or 8; pair: the 2-SM kernel) that fit on the device at once.
-int resident_clusters(DeviceState& st, int bn, int cluster, bool pair) {
+// Split-K clusters of `cluster` CTAs (2, 4 or 8) that fit on the device at once.
+int resident_clusters(DeviceState& st, int bn, int cluster) {
     int bi = 0;
     while (bi < 4 && kBnChoices[bi] != bn) ++bi;
-    const int ci = pair ? 3 : (cluster == 2 ? 0 : (cluster == 4 ? 1 : 2));
+    const int ci = cluster == 2 ? 0 : (cluster == 4 ? 1 : 2);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (st.clusters[bi][ci] != 0) return st.clusters[bi][ci] > 0 ? st.clusters[bi][ci] : 0;
     }
     int n = 0;
     cudaError_t e = cudaErrorInvalidValue;
-    if (pair) {
-        switch (bn) {
-            case 128: e = fg::max_active_clusters<128, false, true>(2, &n); break;
-            case 224: e = fg::max_active_clusters<224, false, true>(2, &n); break;
-            case 256: e = fg::max_active_clusters<256, false, true>(2, &n); break;
-            default: break;
-        }
-    } else {
-        switch (bn) {
-            case 64: e = fg::max_active_clusters<64, false, false, true>(cluster, &n); break;
-            case 128: e = fg::max_active_clusters<128, false, false, true>(cluster, &n); break;
-            case 192: e = fg::max_active_clusters<192, false, false, true>(cluster, &n); break;
-            case 224: e = fg::max_active_clusters<224, false, false, true>(cluster, &n); break;
-            default: e = fg::max_active_clusters<256, false, false, true>(cluster, &n); break;
-        }
+    switch (bn) {
+        case 64: e = fg::max_active_clusters<64, fg::kMajNT, true>(cluster, &n); break;
+        case 128: e = fg::max_active_clusters<128, fg::kMajNT, true>(cluster, &n); break;
+        case 192: e = fg::max_active_clusters<192, fg::kMajNT, true>(cluster, &n); break;
+        case 224: e = fg::max_active_clusters<224, fg::kMajNT, true>(cluster, &n); break;
+        default: e = fg::max_active_clusters<256, fg::kMajNT, true>(cluster, &n); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -171,12 +162,23 @@ bool encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
     return r == CUDA_SUCCESS;
 }
 
-// C/D maps of a [rows][N] output: boxes of 32 rows x 128 bytes (32 FP32 or 64 BF16
-// columns), 128-byte swizzle, matching the epilogue's shared-memory slots.
-bool encode_out_2d(CUtensorMap* map, const void* base, int n, long long rows, bool f32) {
+// C/D maps of a [rows][N] output: boxes of box_rows rows x 128 bytes (32 FP32 or 64 BF16
+// columns), 128-byte swizzle, matching the epilogue's shared-memory slots (128 rows for a
+// whole block, 32 rows for one epilogue warp's rows).
+bool encode_out_2d(CUtensorMap* map, const void* base, int n, long long rows, bool f32, uint32_t box_rows) {
     const uint32_t esz = f32 ? 4 : 2;
     return encode_2d(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base,
-                     (uint64_t)n, (uint64_t)rows, (uint64_t)n * esz, 128 / esz, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+                     (uint64_t)n, (uint64_t)rows, (uint64_t)n * esz, 128 / esz, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// D map of a [rows][N] output: one epilogue warp's 32 rows per box.
+bool encode_d_maps(fg::GemmMaps& gm, const void* d, int n, long long rows, bool f32) {
+    return encode_out_2d(&gm.d, d, n, rows, f32, 32);
+}
+
+// C map of a [rows][N] FP32 input: one epilogue warp's 32 rows per box.
+bool encode_c_maps(fg::GemmMaps& gm, const float* c, int n, long long rows) {
+    return encode_out_2d(&gm.c, c, n, rows, true, 32);
 }
 
 bool print_configs() {
@@ -255,7 +257,7 @@ DenseTiling choose_dense_tiling(DeviceState& st, int num_mb, int n, int k, int s
             if (fs && s != fs) continue;
             if (tiles * s > sms) continue;
             if (!fs && nkb < 2 * s) continue;
-            if (tiles > resident_clusters(st, bn, s, false)) continue;
+            if (tiles > resident_clusters(st, bn, s)) continue;
             const double t = ceil_div(nkb, s) * t_kb_us(bn) + t_x_us(s);
             if (fs || t < best_t) {
                 best = DenseTiling{bn, s};
@@ -274,6 +276,12 @@ int choose_bn_tn(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     return row_blocks * ceil_div(n, 256) >= sms ? 256 : 128;
 }
 
+// L2 prefetch of a single-tile CTA's B before its grid-dependency wait (FG_PREFETCH_B=0 disables it).
+int prefetch_b_enabled() {
+    const char* e = std::getenv("FG_PREFETCH_B");
+    return e && e[0] == '0' ? 0 : 1;
+}
+
 void fill_common(GemmParams& p, const DeviceState& st) {
     p.split = 1;
     p.a_box_rows = 128;
@@ -283,35 +291,15 @@ void fill_common(GemmParams& p, const DeviceState& st) {
     p.pdl = g_pdl;
 }
 
-int launch_nt_pair(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
-    cudaError_t e;
-    switch (bn) {
-        case 128: e = fg::launch_gemm<128, false, true>(p, gm, grid, s); break;
-        case 224: e = fg::launch_gemm<224, false, true>(p, gm, grid, s); break;
-        default: e = fg::launch_gemm<256, false, true>(p, gm, grid, s); break;
-    }
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return FG_ERR_CUDA;
-    }
-    return FG_OK;
-}
-
-// CTA-pair (2-SM MMA) path for the dense GEMM: FG_2SM=1 forces it, FG_2SM=0 disables it.
-int use_pair_mode() {
-    const char* e = std::getenv("FG_2SM");
-    return e && e[0] == '1';
-}
-
 int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
     if (p.split > 1) {
         switch (bn) {
-            case 64: e = fg::launch_gemm<64, false, false, true>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, false, false, true>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, false, false, true>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, false, false, true>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, false, false, true>(p, gm, grid, s); break;
+            case 64: e = fg::launch_gemm<64, fg::kMajNT, true>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, fg::kMajNT, true>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, fg::kMajNT, true>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, fg::kMajNT, true>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, fg::kMajNT, true>(p, gm, grid, s); break;
         }
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -320,11 +308,11 @@ int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cud
         return FG_OK;
     }
     switch (bn) {
-        case 64: e = fg::launch_gemm<64, false>(p, gm, grid, s); break;
-        case 128: e = fg::launch_gemm<128, false>(p, gm, grid, s); break;
-        case 192: e = fg::launch_gemm<192, false>(p, gm, grid, s); break;
-        case 224: e = fg::launch_gemm<224, false>(p, gm, grid, s); break;
-        default: e = fg::launch_gemm<256, false>(p, gm, grid, s); break;
+        case 64: e = fg::launch_gemm<64, fg::kMajNT>(p, gm, grid, s); break;
+        case 128: e = fg::launch_gemm<128, fg::kMajNT>(p, gm, grid, s); break;
+        case 192: e = fg::launch_gemm<192, fg::kMajNT>(p, gm, grid, s); break;
+        case 224: e = fg::launch_gemm<224, fg::kMajNT>(p, gm, grid, s); break;
+        default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -346,7 +334,7 @@ bool encode_swiglu_b(CUtensorMap* map, const void* b, int K, int I, int G) {
 }
 
 int launch_swiglu(const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
-    const cudaError_t e = fg::launch_gemm<256, fg::kMajNT, false, false, true>(p, gm, grid, s);
+    const cudaError_t e = fg::launch_gemm<256, fg::kMajNT, false, true>(p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -399,21 +387,15 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
-    const bool pair = use_pair_mode() && num_mb >= 2 && sms >= 2;
-    DenseTiling tiling{0, 1};
-    if (pair) {
-        const int b0 = choose_bn_nt(num_mb, N, sms, c != nullptr);
-        tiling.bn = (b0 == 256 || b0 == 224 || b0 == 128) ? b0 : 224;
-    } else {
-        tiling = choose_dense_tiling(*st, num_mb, N, K, sms, c != nullptr);
-    }
+    const DenseTiling tiling = choose_dense_tiling(*st, num_mb, N, K, sms, c != nullptr);
     const int bn = tiling.bn;
     GemmParams p{};
     fill_common(p, *st);
     p.kind = fg::kDense;
     p.M = M; p.N = N; p.K = K; p.G = 1;
     p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
-    p.num_mb = pair ? ceil_div(num_mb, 2) : num_mb;   // pair mode: pairs of 128-row blocks
+    p.c_in_d = c != nullptr && static_cast<const void*>(c) == d;
+    p.num_mb = num_mb;
     p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
@@ -423,32 +405,23 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     p.split = tiling.split;
     // a single row block of at most 64 rows: load only those rows of A (the MMA still
     // reads 128 rows of shared memory; rows past M produce accumulator rows never stored)
-    p.a_box_rows = (!pair && M <= 64) ? 64 : 128;
+    p.a_box_rows = M <= 64 ? 64 : 128;
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, pair ? bn / 2 : bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
+        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_d_maps(gm, d, N, M, p.d_f32) || (c && !encode_c_maps(gm, c, N, M)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
-    int grid;
-    if (pair) {
-        // whole pairs only, and no more pairs than can be resident at once
-        int units = sms / 2;
-        const int rc2 = resident_clusters(*st, bn, 2, true);
-        if (rc2 > 0 && rc2 < units) units = rc2;
-        grid = (int)(tiles < units ? tiles : units) * 2;
-    } else if (p.split > 1) {
-        grid = (int)tiles * p.split;    // one tile per cluster, all clusters resident
-    } else {
-        grid = (int)(tiles < sms ? tiles : sms);
-    }
+    // split-K: one tile per cluster, all clusters resident
+    const int grid = p.split > 1 ? (int)tiles * p.split : (int)(tiles < sms ? tiles : sms);
+    // one tile per CTA (or cluster): its B can be prefetched into L2 before the dependency wait
+    p.prefetch_b = g_pdl && (p.split > 1 || tiles <= sms) && prefetch_b_enabled();
     if (print_configs())
-        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d%s\n", M, N, K, bn,
-                     p.split, tiles, grid, pair ? " (CTA pairs)" : "");
-    if (pair) return launch_nt_pair(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d\n", M, N, K, bn,
+                     p.split, tiles, grid);
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -486,12 +459,12 @@ int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const 
     p.b_gstride_k = K;
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    CUtensorMap &ma = gm.a, &mb = gm.b, &md = gm.d;
+    CUtensorMap &ma = gm.a, &mb = gm.b;
     const bool b_ok = b_nmajor
         ? encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, (uint64_t)G * K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
         : encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !b_ok || !encode_out_2d(&md, d, N, M_total, p.d_f32))
+        !b_ok || !encode_d_maps(gm, d, N, M_total, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
@@ -530,6 +503,7 @@ int dense_mn(int maj, int M, int N, int K, const uint8_t* a, const int32_t* sfa,
     p.kind = fg::kDense;
     p.M = M; p.N = N; p.K = K; p.G = 1;
     p.d_f32 = d_dtype == FG_F32; p.has_c = c != nullptr;
+    p.c_in_d = c != nullptr && static_cast<const void*>(c) == d;
     p.num_mb = num_mb;
     p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
@@ -540,14 +514,14 @@ int dense_mn(int maj, int M, int N, int K, const uint8_t* a, const int32_t* sfa,
     p.a_box_rows = (!a_mn && M <= 64) ? 64 : 128;
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c;
     const bool a_ok = a_mn
         ? encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, M, K, M, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
         : encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     const bool b_ok = b_mn
         ? encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
         : encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!a_ok || !b_ok || !encode_out_2d(&md, d, N, M, p.d_f32) || (c && !encode_out_2d(&mc, c, N, M, true)))
+    if (!a_ok || !b_ok || !encode_d_maps(gm, d, N, M, p.d_f32) || (c && !encode_c_maps(gm, c, N, M)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
@@ -619,11 +593,11 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     fill_common(p, *st);
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c, &md = gm.d;
+    CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_out_2d(&md, d, N, (long long)G * M_max, p.d_f32))
+        !encode_d_maps(gm, d, N, (long long)G * M_max, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)G * p.num_mb * p.num_nb;   // upper bound
     const int grid = (int)(tiles < sms ? tiles : sms);
@@ -774,6 +748,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     p.kind = fg::kKGrouped;
     p.M = M; p.N = N; p.K = K_total; p.G = G;
     p.d_f32 = 1; p.has_c = c != nullptr;
+    p.c_in_d = c != nullptr && c == d;
     p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(N);

@@ -16,15 +16,31 @@
 // K-groups; it is copied to TMEM unchanged and the MMA's scale-factor byte selector
 // picks byte (g mod 4).
 //
-// Warp roles (224 threads):
-//   warp 0      TMA producer: A tiles into a ring of shared-memory stages
+// Warp roles (320 threads):
+//   warps 0, 8  TMA producers of A tiles into a ring of shared-memory stages (even / odd
+//               stages)
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
-//   warp 2      scale loader: packed UE8M0 words copied by cp.async into the tcgen05.cp
-//               layout of each stage, completion tracked by the stage's mbarrier; lane 0
-//               also issues the stage's B tile (a warp's TMA loads complete one after
-//               another, so A and B come from different warps)
-//   warps 3..6  epilogue: TMEM -> registers, + C (TMA-prefetched into shared memory),
-//               -> BF16/FP32 -> swizzled shared-memory slot -> TMA store
+//   warps 2, 9  TMA producers of B tiles (even / odd stages).  Measured on GB300: the TMA
+//               loads one warp issues complete one after another, about 0.34 us each
+//               from L2 whatever the box size (4-32 KB), while loads of different warps
+//               proceed in parallel; so each operand streams from two warps.
+//   warp 3      scale loader: the packed UE8M0 words of each tile (one word row per four
+//               K-groups), copied by the whole warp with 4-byte cp.async straight into the
+//               tcgen05.cp 32x4 atom layout of the stage that starts the word row; every lane
+//               arrives on every stage's full barrier once its copies have landed, so the MMA
+//               issuer waits once per stage for operands and scales, and this warp never
+//               waits for load latency
+//   warps 4..7  epilogue: TMEM -> registers, + C -> BF16/FP32 -> TMA store, each warp on
+//               its own 32 rows: C chunks land in slots of their own, loaded ahead by lane 0
+//               and refilled as soon as read; D chunks leave from store slots through TMA
+//               stores issued by lane 1 (the two TMA streams of a warp proceed side by side).
+//               When D is C itself (in-place accumulation) no C is loaded: the accumulator
+//               chunk leaves through a TMA reduce-add, and L2 adds it onto D.
+// The MMA issuer is the throughput limit of narrow tiles (measured on GB300: ~55 clocks to
+// issue one tcgen05.mma and ~200 to test an mbarrier, against 448 clocks of tensor work per
+// 128 x 224 x 128 K-group), so its loop is lean: descriptors are precomputed per stage, and
+// when the next two stages have both landed (two pipelined non-blocking tests) it issues
+// both stages' MMAs after one round of waiting.
 // Accumulators are double-buffered in TMEM when two fit next to the scale slots
 // (BN <= 224), so the epilogue of one tile overlaps the MMAs of the next.
 //
@@ -66,14 +82,19 @@ enum : int {
     kChkKSegments = 4,         // ks not multiples of 128 / negative / wrong sum
     kChkSplit = 5,             // split-K launch without one tile per cluster
     kWaitProducer = 1, kWaitMma = 2, kWaitScales = 3, kWaitEpilogue = 4, kWaitDrain = 5,
-    kWaitEpilogueC = 6, kWaitExchange = 7,
+    kWaitEpilogueC = 6, kWaitExchange = 7, kWaitScaleSlot = 8, kWaitProducerB = 9, kWaitEpilogueSync = 10,
+    kWaitEpilogueCFree = 11,
 };
 
 constexpr int kMaxGroups = 256;   // masked / K-grouped groups held in shared memory
 constexpr int kSmemLimit = 232448;
+constexpr int kGemmThreads = 320;
+constexpr int kEpiWarp0 = 4;      // first epilogue warp
+constexpr int kEpiThread0 = 32 * kEpiWarp0;
 
 // Tensor maps of one launch (a kernel parameter, so the TMA unit reads them from
-// parameter space): A and B operand tiles, C and D 32-row x 128-byte epilogue boxes.
+// parameter space): A and B operand tiles, C and D in 32-row x 128-byte boxes (one epilogue
+// warp's chunk).
 struct GemmMaps {
     CUtensorMap a, b, c, d;
 };
@@ -83,6 +104,9 @@ struct GemmParams {
     int M, N, K;           // dense M,N,K | contiguous M_total | masked M_max | K-grouped M,N,K_total
     int G;
     int d_f32, has_c;
+    int c_in_d;            // C is D itself (in-place accumulation): D += A @ B by TMA reduce-add
+    int prefetch_b;        // dense, one tile per CTA: prefetch the tile's B into L2 before the
+                           // grid-dependency wait
     int num_mb, num_nb;    // tile grid of one group
     const int32_t* sfa;
     const int32_t* sfb;
@@ -107,7 +131,7 @@ struct GemmParams {
     int debug_stall;
 };
 
-template <int BN, bool k2Sm = false, bool kSplit = false>
+template <int BN, bool kSplit = false, bool kSwiGLU = false>
 struct TileCfg {
     static constexpr int kBM = 128, kBK = 128;
     static constexpr int kSfbAtoms = (BN + 127) / 128;
@@ -116,41 +140,52 @@ struct TileCfg {
     static constexpr int kSfCol0 = (kNumAcc * BN + 15) / 16 * 16;
     static_assert(kSfCol0 + 16 + kSfCols <= 512, "TMEM columns");
     static constexpr int kABytes = kBM * kBK;              // 16 KB
-    static constexpr int kBRows = k2Sm ? BN / 2 : BN;       // B rows held by this CTA
-    static constexpr int kBBytes = kBRows * kBK;
+    static constexpr int kBBytes = BN * kBK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    // Scale words of a stage (used by the stages that start a packed word row, four
+    // K-groups): the 128 A rows' words and the words of the BN B rows, each as 32x4 atoms of
+    // 512 bytes.
     static constexpr int kSfaBytes = 512;
     static constexpr int kSfbBytes = kSfbAtoms * 512;
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-    // Epilogue: per warp, kSlots shared-memory slots of 32 rows x 128 bytes.
-    // C-prefetch depth against pipeline stages: wide tiles keep four slots per warp (their
-    // epilogue streams the most C), narrow tiles and CTA pairs take more stages instead.
-    // Split-K variants exchange through the operand ring and need no slots: their shared
-    // memory goes to pipeline stages.
-    static constexpr int kSlots = kSplit ? 0 : (k2Sm ? 2 : (BN >= 256 ? 1 : (BN >= 192 ? 4 : 2)));
+    static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
+    // Epilogue, per warp: kCSlots slots where C chunks land (refilled as soon as read) and
+    // kDSlots slots from which D chunks are stored; each slot is 32 rows x 128 bytes (one
+    // chunk: 32 FP32 or 64 BF16 columns).  Split-K variants exchange through the operand
+    // ring and use no slots; the SwiGLU variant stages one chunk of codes; tiles too wide
+    // for two accumulators rarely take C and give the space to pipeline stages (their C,
+    // if any, lands in the store slot).
+    // (measured on GB300: the mainloop of these kernels is bound by the bytes its ring holds
+    // in flight, so narrow tiles give the space to a fifth stage)
+    static constexpr int kCSlots = (kSplit || kSwiGLU) ? 0 : (BN >= 256 ? 0 : (BN >= 192 ? 3 : 2));
+    static constexpr int kDSlots = kSplit ? 0 : 1;
     static constexpr int kSlotBytes = 4096;
-    static constexpr int kEpiBytes = 4 * kSlots * kSlotBytes;
+    static constexpr int kEpiBytes = 4 * (kCSlots + kDSlots) * kSlotBytes;
     static constexpr int kMiscBytes = 1024 + 2 * (kMaxGroups + 1) * 4;   // barriers etc. + group tables
-    static constexpr int kStages0 = (kSmemLimit - 1024 - kEpiBytes - kMiscBytes) / kStageBytes;
+    static constexpr int kStages0 = (kSmemLimit - 1024 - kEpiBytes - kMiscBytes) / (kStageBytes + kSfSlotBytes);
     static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffEpi = kOffB + kStages * kBBytes;                 // 1024-aligned
-    static constexpr int kOffSfa = kOffEpi + kEpiBytes;
-    static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1 + 4 * kSlots + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;                   // tmem addr, abort flag
-    static constexpr int kOffSched = kOffMisc + 16;                           // int[kMaxGroups + 1]
+    static constexpr int kOffCSlots = kOffEpi;
+    static constexpr int kOffDSlots = kOffEpi + 4 * kCSlots * kSlotBytes;
+    static constexpr int kOffSf = kOffEpi + kEpiBytes;
+    static constexpr int kOffBar = kOffSf + kStages * kSfSlotBytes;
+    // per epilogue warp: C landed in one of its C slots / in one of its store slots
+    static constexpr int kNumCBars = 4 * (kCSlots + kDSlots);
+    static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1 + kNumCBars + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;                   // tmem addr, abort flag, row flags
+    static constexpr int kOffSched = kOffMisc + 32;                           // int[kMaxGroups + 1]
     static constexpr int kOffCnt = kOffSched + (kMaxGroups + 1) * 4;
     static constexpr int kSmemBytes = kOffCnt + kMaxGroups * 4 + 1024;       // + alignment slack
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128 (and 32-column chunks)");
     static_assert(kStages >= 2, "pipeline depth");
-    static_assert(kNumBars * 8 <= 1024 - 16, "barrier area");
+    static_assert(kNumBars * 8 <= 1024 - 32, "barrier area");
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    static_assert(kOffSf % 512 == 0 && kSfSlotBytes % 512 == 0, "scale atoms 512-byte aligned");
     // Split-K exchange buffer: the FP32 partial tile, rows padded by 16 bytes, in the
     // operand ring (idle once the cluster's single tile has been accumulated).
     static constexpr int kXStride = BN + 4;
-    static_assert(kStages * (kABytes + kBBytes) >= kBM * kXStride * 4, "split-K exchange buffer");
+    static_assert(!kSplit || kStages * (kABytes + kBBytes) >= kBM * kXStride * 4, "split-K exchange buffer");
 };
 
 struct Tile {
@@ -185,7 +220,8 @@ __device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
     if (kCluster) return mbar_try_wait_cluster(bar, parity);
     return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity);
 }
-// kCluster: the barrier is also arrived on from the paired CTA (acquire at cluster scope).
+// kCluster: the barrier is also arrived on from another CTA of the cluster (acquire at
+// cluster scope).
 template <bool kCluster = false, bool kSleep = true>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitCtl& w, int where) {
     if (try_wait_scoped<kCluster, kSleep>(bar, parity)) return true;
@@ -211,14 +247,13 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
-// In CTA-pair mode (dense only) a tile index names a pair of 128-row blocks; `rank`
-// selects this CTA's block and its half of the B rows.
+// rank: this CTA's rank in its split-K cluster (its share of the K-groups).
 // scan: the caller is a whole warp walking the tiles together (the scale loader); it
 // checks that a contiguous block whose first row is padding (-1) names no group in any
 // later row (such a block is skipped, so its rows would silently stay unwritten).
 template <int BN>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const int* sched,
-                                            const int* cnt, int& cursor, int rank, bool pair, int split,
+                                            const int* cnt, int& cursor, int rank, int split,
                                             bool scan) {
     Tile tl;
     tl.skip = false;
@@ -229,11 +264,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, int t, const in
     tl.d_z = 0;
     tl.b_krow = 0;
     if (p.kind == kDense) {
-        const int mbq = t % p.num_mb, nb = t / p.num_mb;
-        const int mb = pair ? 2 * mbq + rank : mbq;
+        const int mb = t % p.num_mb, nb = t / p.num_mb;
         tl.n0 = nb * BN;
         tl.a_coord = mb * 128;
-        tl.b_coord = pair ? tl.n0 + rank * (BN / 2) : tl.n0;
+        tl.b_coord = tl.n0;
         tl.valid_rows = min(128, p.M - mb * 128);
         tl.d_row = mb * 128;
         tl.sfa_row = mb * 128;
@@ -306,12 +340,11 @@ struct TileIter {
     int cursor;
     int stride;
     int rank;
-    bool pair;
     int split;
     __device__ __forceinline__ bool next(const GemmParams& p, int total, const int* sched, const int* cnt,
                                          Tile& tl, bool scan = false) {
         while (t < total) {
-            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, pair, split, scan);
+            tl = decode_tile<BN>(p, t, sched, cnt, cursor, rank, split, scan);
             t += stride;
             if (!tl.skip) return true;
         }
@@ -319,12 +352,11 @@ struct TileIter {
     }
 };
 
-// Tiles of this CTA: blockIdx.x + i * gridDim.x, or per cluster (CTA pair, split-K
-// cluster) when clusters share tiles.
-template <int BN, bool k2Sm>
+// Tiles of this CTA: blockIdx.x + i * gridDim.x, or per split-K cluster when clusters share
+// tiles.
+template <int BN>
 __device__ __forceinline__ TileIter<BN> tiles_of_cta(int rank, int split) {
-    if (k2Sm) return TileIter<BN>{static_cast<int>(blockIdx.x >> 1), 0, static_cast<int>(gridDim.x >> 1), rank, true, 1};
-    return TileIter<BN>{static_cast<int>(blockIdx.x) / split, 0, static_cast<int>(gridDim.x) / split, rank, false, split};
+    return TileIter<BN>{static_cast<int>(blockIdx.x) / split, 0, static_cast<int>(gridDim.x) / split, rank, split};
 }
 
 // ------------------------------------------------------------ split-K exchange
@@ -351,7 +383,7 @@ __device__ __noinline__ bool split_k_tile(const SplitTile st, float* xb, uint32_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;                                // TMEM sub-partition of this warp
     const int row = q * 32 + lane;
-    const int te = static_cast<int>(threadIdx.x) - 96;     // 0..127 over the epilogue warps
+    const int te = static_cast<int>(threadIdx.x) - 32 * kEpiWarp0;   // 0..127 over the epilogue warps
     constexpr int kB = 4;                                  // slice items (float4 groups) per thread and pass
     const int vr = st.valid_rows;
     const int w = BN / split;
@@ -463,29 +495,26 @@ __device__ __forceinline__ float swiglu_value(uint32_t gate, uint32_t up) {
     return __fdividef(x, 1.0f + __expf(-x)) * __uint_as_float(up);
 }
 
-template <int BN, int kMaj, bool k2Sm, bool kSplit, bool kSwiGLU>
-__global__ void __launch_bounds__(224, 1)
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU>
+__global__ void __launch_bounds__(kGemmThreads, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_a = maps.a;
     const CUtensorMap& tm_b = maps.b;
     const CUtensorMap& tm_c = maps.c;
     const CUtensorMap& tm_d = maps.d;
     constexpr bool kAmn = (kMaj & 1) != 0, kBmn = (kMaj & 2) != 0;
-    static_assert(!(kMaj != kMajNT && k2Sm), "CTA pairs are used by the NT kernels only");
-    static_assert(!(kSplit && (kMaj != kMajNT || k2Sm)), "split-K clusters are a dense NT variant");
+    static_assert(!(kSplit && kMaj != kMajNT), "split-K clusters are a dense NT variant");
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
-    static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !k2Sm && !kSplit),
+    static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
-    using C = TileCfg<BN, k2Sm, kSplit>;
+    using C = TileCfg<BN, kSplit, kSwiGLU>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTA pair: rank 0 (leader) issues the MMAs for both CTAs; rank 1 holds the other 128 rows.
-    // Split-K cluster: rank r runs the r-th share of the K-groups (every CTA is its own leader).
+    // Split-K cluster: rank r runs the r-th share of the K-groups.
     const int split = kSplit ? p.split : 1;   // a compile-time 1 outside the split-K variant
-    const int rank = (k2Sm || split > 1) ? static_cast<int>(cluster_ctarank()) : 0;
-    const bool leader = !k2Sm || rank == 0;
+    const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
 
     const uint32_t bar0 = sbase + C::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -493,10 +522,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + C::kNumAcc + b); };
     const uint32_t mma_drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc);
-    auto cfull_bar = [&](int ew, int slot) {
-        return bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + ew * C::kSlots + slot);
-    };
-    const uint32_t xfull_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + 4 * C::kSlots);
+    // epilogue slot barriers of warp ew: C landed in its C slot i / in its store slot j
+    const uint32_t ebar0 = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1);
+    auto cfull_bar = [&](int ew, int i) { return ebar0 + 8u * (ew * (C::kCSlots + C::kDSlots) + i); };
+    auto dcfull_bar = [&](int ew, int j) { return ebar0 + 8u * (ew * (C::kCSlots + C::kDSlots) + C::kCSlots + j); };
+    const uint32_t xfull_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kNumAcc + 1 + C::kNumCBars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     int* sched = reinterpret_cast<int*>(smem + C::kOffSched);
@@ -505,20 +535,17 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     // ---------------------------------------------------------------- prologue
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            // One CTA: producer arrive (A bytes), scale-loader lane 0 arrive (B bytes), 32
-            // scale-loader lanes (cp.async).  Pair mode: producer arrive (TMA bytes of both
-            // CTAs), 32 scale-loader lanes and the peer's scale relay; the peer's own barrier
-            // counts only its scale-loader lanes.
-            mbar_init(full_bar(s), k2Sm ? (leader ? 34 : 32) : 34);
+            // the A and the B producer each arrive (with their bytes) and the 32 scale-loader
+            // lanes arrive once their copies have landed
+            mbar_init(full_bar(s), 34);
             mbar_init(empty_bar(s), 1);    // tcgen05.commit of the MMA issuer
         }
         for (int b = 0; b < C::kNumAcc; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), k2Sm && leader ? 8 : 4);   // one arrive per epilogue warp (of both CTAs)
+            mbar_init(acce_bar(b), 4);   // one arrive per epilogue warp
         }
         mbar_init(mma_drain_bar, 1);
-        if constexpr (C::kSlots > 0)
-            for (int i = 0; i < 4 * C::kSlots; ++i) mbar_init(cfull_bar(i / C::kSlots, i % C::kSlots), 1);
+        for (int i = 0; i < C::kNumCBars; ++i) mbar_init(ebar0 + 8u * i, 1);   // TMA bytes of a C chunk
         mbar_init(xfull_bar, 4 * split);   // split-K: every epilogue warp of the cluster
         *abort_flag = 0;
         fence_mbar_init();
@@ -527,25 +554,38 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             tma_prefetch_map(&tm_b);
         }
         tma_prefetch_map(&tm_d);
-        if (p.has_c) tma_prefetch_map(&tm_c);
+        if (p.has_c && !p.c_in_d) tma_prefetch_map(&tm_c);
     }
     if (warp == 1) {
-        if constexpr (k2Sm) {   // collective: one warp of each CTA of the pair
-            tmem_alloc_pair(smem_u32(tmem_slot), 512);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(tmem_slot), 512);
-            tmem_relinquish();
-        }
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
     }
     tc_fence_before();
     // the cluster's barriers are initialised before any CTA of it arrives on them remotely
-    if (k2Sm || split > 1) cluster_sync();
+    if (split > 1) cluster_sync();
     else __syncthreads();
     tc_fence_after();
-    // Nothing above touched global memory (the tensor maps are kernel parameters), so the
-    // set-up overlaps the previous grid's tail under a programmatic launch; here its results
-    // become visible.
+    // While the previous grid of the stream finishes (programmatic launch), a CTA that owns a
+    // single dense tile asks L2 for that tile's B (the weights) with tensor-map prefetches
+    // spread over four lanes.  A prefetch moves data from HBM into L2 only: nothing reaches
+    // this SM before the dependency wait, and L2 is where every write of the previous grid
+    // lands, so the loads after the wait see that grid's data whatever it wrote.
+    if (p.prefetch_b && warp == 2 && lane < 4 && p.kind == kDense) {
+        TileIter<BN> pit = tiles_of_cta<BN>(rank, split);
+        Tile ptl;
+        if (pit.next(p, p.num_mb * p.num_nb, sched, cnt, ptl)) {
+            for (int kb = lane; kb < ptl.nkb; kb += 4) {
+                const int kc = (ptl.kb0 + kb) * 128;
+                if constexpr (!kBmn) tma_prefetch_l2_2d(&tm_b, kc, ptl.b_coord);
+                else
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h) tma_prefetch_l2_2d(&tm_b, ptl.n0 + h * 128, kc);
+            }
+        }
+    }
+    // Nothing above read global memory into the SM (the tensor maps are kernel parameters),
+    // so the set-up overlaps the previous grid's tail under a programmatic launch; here its
+    // results become visible.
     grid_dependency_wait();
     if (threadIdx.x == 0) grid_launch_dependents();
     // Group tables for the masked (tile prefix) and K-grouped (K-group prefix) layouts.
@@ -602,18 +642,24 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
 
     const WaitCtl wctl{abort_flag, p.status, p.timeout_ns};
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 8) {
+        // ----------------------------------------------------- TMA producers of A
+        // warp 0 fills the even stages of the global stage sequence, warp 8 the odd ones
         if (lane == 0) {
+            const uint32_t par = warp == 0 ? 0u : 1u;
             int s = 0;
-            uint32_t ph = 0;
-            bool stall = p.debug_stall != 0 && leader;
+            uint32_t ph = 0, g = 0;
+            bool stall = p.debug_stall != 0 && par == 0;
             uint32_t armed = 0, armed_par = 0;   // per-stage: armed at least once / parity
             bool aborted = false;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
+            TileIter<BN> it = tiles_of_cta<BN>(rank, split);
             Tile tl;
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
-                for (int kb = 0; kb < tl.nkb; ++kb) {
+                for (int kb = 0; kb < tl.nkb; ++kb, ++g) {
+                    if ((g & 1u) != par) {
+                        if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
                     if (!wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitProducer)) { aborted = true; break; }
                     if (stall) {
                         stall = false;   // leave this stage unarmed: the MMA issuer times out
@@ -621,12 +667,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         const uint32_t fb = full_bar(s);
                         const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
                         const int kc = (tl.kb0 + kb) * 128;
-                        if constexpr (k2Sm) {
-                            // both CTAs' tiles complete on the leader's barrier; B comes from
-                            // the scale-loader warp
-                            if (leader) mbar_arrive_expect_tx(fb, 2 * (C::kABytes + C::kBBytes));
-                            tma_load_2d_pair(sa, &tm_a, map_shared_rank(fb, 0), kc, tl.a_coord);
-                        } else if (!kAmn) {   // B is loaded by the scale-loader warp
+                        if constexpr (!kAmn) {
                             mbar_arrive_expect_tx(fb, p.a_box_rows * C::kBK);
                             tma_load_2d(sa, &tm_a, fb, kc, tl.a_coord);
                         } else {              // A [K][M]: one 128 (M) x 128 (K) box
@@ -639,139 +680,119 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (leader && (aborted || *abort_flag)) {
+            if (aborted || *abort_flag) {
                 // Bounded drain of loads that may still be landing in shared memory.
                 for (int i = 0; i < C::kStages; ++i)
                     if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && k2Sm && !leader) {
-            // Peer of a CTA pair: the leader's MMAs read this CTA's shared memory, so the
-            // leader must learn when this CTA's scale words have landed: relay each stage's
-            // completion (local barrier, 32 scale-loader lanes) to the leader's stage barrier.
-            int s = 0;
-            uint32_t ph = 0;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
-            Tile tl;
-            bool aborted = false;
-            while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
-                for (int kb = 0; kb < tl.nkb; ++kb) {
-                    if (!wait_bar(full_bar(s), ph, wctl, kWaitScales)) { aborted = true; break; }
-                    fence_proxy_async_smem();
-                    mbar_arrive_remote(map_shared_rank(full_bar(s), 0));
-                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
-                }
-            }
-        } else if (lane == 0) {
-            constexpr uint32_t kIdesc = make_idesc_mxf8(k2Sm ? 256 : 128, BN, kAmn, kBmn);
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = make_idesc_mxf8(128, BN, kAmn, kBmn);
+            // Shared-memory descriptors of stage 0; a stage's descriptor adds its offset in
+            // 16-byte units to the start-address field (shared addresses stay below 2^18, so
+            // the 14-bit field never carries).  K step j of a stage: K-major operands advance
+            // 32 bytes along the 128-byte swizzled rows, MN-major ones 4 KB (8 K rows of 128-wide
+            // atoms 16 KB apart).
+            const uint64_t a_desc0 = kAmn ? make_sdesc(sbase + C::kOffA, 16384, 1024, kLayoutSw128)
+                                          : make_sdesc(sbase + C::kOffA, 0, 1024, kLayoutSw128);
+            const uint64_t b_desc0 = kBmn ? make_sdesc(sbase + C::kOffB, 16384, 1024, kLayoutSw128)
+                                          : make_sdesc(sbase + C::kOffB, 0, 1024, kLayoutSw128);
+            constexpr uint32_t kAStep = kAmn ? 4096 / 16 : 32 / 16, kBStep = kBmn ? 4096 / 16 : 32 / 16;
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
             uint32_t kcount = 0;    // scale-word copies issued (selects the TMEM scale slot)
             bool aborted = false;
-            TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
+            TileIter<BN> it = tiles_of_cta<BN>(rank, split);
             Tile tl;
+            // one stage: the scale words it carries (if it starts a packed word row) to TMEM,
+            // its four MMAs, and the commit that frees it
+            auto issue_stage = [&](int kb, uint32_t d_t) {
+                const uint32_t sf_id = static_cast<uint32_t>(tl.kb0 + kb) & 3u;
+                if (kb == 0 || sf_id == 0) {
+                    // A packed word holds the scales of four consecutive K-groups: copy it at the
+                    // tile's first K-group and at every fourth global K-group, alternating between
+                    // two TMEM slots (the copy of the next word never overwrites one still read by
+                    // MMAs in flight: tcgen05 operations of one thread execute in issue order).
+                    ++kcount;
+                    const uint32_t sfa_n = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                    const uint32_t ssfa = sbase + C::kOffSf + s * C::kSfSlotBytes;
+                    fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
+                    tc_cp_32x128b_warpx4(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
+#pragma unroll
+                    for (int i = 0; i < C::kSfbAtoms; ++i)
+                        tc_cp_32x128b_warpx4(sfa_n + 4 + 4 * i, make_sdesc(ssfa + C::kSfaBytes + 512 * i, 0, 128, kLayoutNone));
+                }
+                const uint32_t sfa_t = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                const uint32_t sfb_t = sfa_t + 4;
+                const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, sf_id);
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * C::kABytes) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * C::kBBytes) >> 4);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tc_mma_mxf8(d_t, ad + kAStep * j, bd + kBStep * j, idesc, sfa_t, sfb_t, (kb | j) != 0);
+                tc_commit(empty_bar(s));
+                if (++s == C::kStages) { s = 0; ph ^= 1u; }
+            };
             while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
-                if (!wait_bar<k2Sm>(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
+                if (!wait_bar(acce_bar(acc), acc_ph ^ 1u, wctl, kWaitMma)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_t = tmem_base + acc * BN;
-                for (int kb = 0; kb < tl.nkb; ++kb) {
-                    if (!wait_bar<k2Sm>(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
+                int kb = 0;
+                while (kb < tl.nkb) {
+                    // the next two stages: two non-blocking tests in flight together
+                    const int s1 = s + 1 == C::kStages ? 0 : s + 1;
+                    const uint32_t ph1 = s + 1 == C::kStages ? ph ^ 1u : ph;
+                    const bool two = kb + 1 < tl.nkb;
+                    const bool r0 = mbar_test_wait(full_bar(s), ph);
+                    bool r1 = two && mbar_test_wait(full_bar(s1), ph1);
+                    if (!r0) {
+                        if (!wait_bar(full_bar(s), ph, wctl, kWaitMma)) { aborted = true; break; }
+                        r1 = two && mbar_test_wait(full_bar(s1), ph1);
+                    }
                     tc_fence_after();
-                    // A packed word holds the scales of four consecutive K-groups, so its copy
-                    // to TMEM serves up to four K-groups: copy at the tile's first K-group and
-                    // at every fourth global K-group, alternating between two TMEM slots (the
-                    // copy of the next word never overwrites one still read by MMAs in flight).
-                    const uint32_t sf_id = static_cast<uint32_t>(tl.kb0 + kb) & 3u;
-                    if (kb == 0 || sf_id == 0) {
-                        ++kcount;
-                        const uint32_t sfa_n = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
-                        const uint32_t ssfa = sbase + C::kOffSfa + s * C::kSfaBytes;
-                        const uint32_t ssfb = sbase + C::kOffSfb + s * C::kSfbBytes;
-                        fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
-                        // pair mode: each CTA's scale words go from its shared memory to its TMEM
-                        if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
-                        else tc_cp_32x128b_warpx4(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
-#pragma unroll
-                        for (int i = 0; i < C::kSfbAtoms; ++i) {
-                            if constexpr (k2Sm) tc_cp_32x128b_warpx4_pair(sfa_n + 4 + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
-                            else tc_cp_32x128b_warpx4(sfa_n + 4 + 4 * i, make_sdesc(ssfb + 512 * i, 0, 128, kLayoutNone));
-                        }
-                    }
-                    const uint32_t sfa_t = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
-                    const uint32_t sfb_t = sfa_t + 4;
-                    const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, sf_id);
-                    const uint32_t sa = sbase + C::kOffA + s * C::kABytes;
-                    const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint64_t ad, bd;
-                        // K-major: 128-byte rows, 8-row swizzle atoms 1024 B apart, +32 B per K step;
-                        // MN-major: 128-byte MN atoms 16 KB apart, 8 K rows per 1024 B, +4 KB per K step
-                        ad = kAmn ? make_sdesc(sa + 4096 * j, 16384, 1024, kLayoutSw128)
-                                  : make_sdesc(sa + 32 * j, 0, 1024, kLayoutSw128);
-                        bd = kBmn ? make_sdesc(sb + 4096 * j, 16384, 1024, kLayoutSw128)
-                                  : make_sdesc(sb + 32 * j, 0, 1024, kLayoutSw128);
-                        if constexpr (k2Sm) tc_mma_mxf8_pair(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
-                        else tc_mma_mxf8(d_t, ad, bd, idesc, sfa_t, sfb_t, (kb | j) != 0);
-                    }
-                    if constexpr (k2Sm) tc_commit_pair_multicast(empty_bar(s));   // frees the stage in both CTAs
-                    else tc_commit(empty_bar(s));
-                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                    issue_stage(kb++, d_t);
+                    if (r1) issue_stage(kb++, d_t);
                 }
                 if (aborted) break;
-                if constexpr (k2Sm) tc_commit_pair_multicast(accf_bar(acc));   // dense: every tile has K-blocks
-                else if (tl.nkb > 0) tc_commit(accf_bar(acc));
+                if (tl.nkb > 0) tc_commit(accf_bar(acc));
                 else mbar_arrive(accf_bar(acc));
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
             // Wait (bounded) until every tensor-core operation issued here has finished.
-            if constexpr (k2Sm) tc_commit_pair_local(mma_drain_bar);
-            else tc_commit(mma_drain_bar);
+            tc_commit(mma_drain_bar);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(mma_drain_bar, 0)) {
                 if (globaltimer_ns() - t0 > p.timeout_ns) { record_status(p.status, kErrTimeout | kWaitDrain); break; }
             }
         }
         __syncwarp();
-    } else if (warp == 2) {
-        // ----------------------------------------------------- scale loader
-        // Per stage that starts a packed word (the tile's first K-group, then every fourth):
-        // the packed UE8M0 word for the tile's 128 A rows and BN B rows, copied with 4-byte
-        // cp.async straight into the tcgen05.cp layout (word
-        // (lane, j) of each 32x4 atom holds MN index j * 32 + lane; rows outside the
-        // problem are zero-filled).  Each lane's copies arrive on the stage's full barrier
-        // when they land, so this warp never waits for global-load latency.
-        // One CTA: lane 0 also issues the stage's B tile.  A warp's TMA loads complete one
-        // after another (measured ~0.25-0.4 us each on GB300 whatever their size), so A and
-        // B from two warps stream in parallel.
-        int s = 0;
-        uint32_t ph = 0;
-        uint32_t armed = 0, armed_par = 0;   // stages whose B load this warp issued / parity
-        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
-        Tile tl;
-        bool aborted = false;
-        while (!aborted && it.next(p, total_tiles, sched, cnt, tl, p.kind == kContiguous)) {
-            const int32_t* pa0 = p.sfa + tl.sfa_g * p.sfa_gstride;
-            const int32_t* pb0 = p.sfb + tl.g * p.sfb_gstride;
-            for (int kb = 0; kb < tl.nkb; ++kb) {
-                // warp-uniform decision: every lane leaves together on abort
-                const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
-                if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                if constexpr (k2Sm) {
-                    // this CTA's half of B, completing on the leader's barrier (armed by its producer)
-                    if (lane == 0)
-                        tma_load_2d_pair(sbase + C::kOffB + s * C::kBBytes, &tm_b, map_shared_rank(full_bar(s), 0),
-                                         (tl.kb0 + kb) * 128, tl.b_coord);
-                    __syncwarp();
-                } else {
-                    if (lane == 0) {
+    } else if (warp == 2 || warp == 9) {
+        // ----------------------------------------------------- TMA producers of B
+        // warp 2 fills the even stages of the global stage sequence, warp 9 the odd ones
+        if (lane == 0) {
+            const uint32_t par = warp == 2 ? 0u : 1u;
+            int s = 0;
+            uint32_t ph = 0, g = 0;
+            uint32_t armed = 0, armed_par = 0;   // stages whose B load this lane issued / parity
+            bool aborted = false;
+            TileIter<BN> it = tiles_of_cta<BN>(rank, split);
+            Tile tl;
+            while (!aborted && it.next(p, total_tiles, sched, cnt, tl)) {
+                for (int kb = 0; kb < tl.nkb; ++kb, ++g) {
+                    if ((g & 1u) != par) {
+                        if (++s == C::kStages) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitProducerB)) { aborted = true; break; }
+                    const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
+                    const int kc = (tl.kb0 + kb) * 128;
+                    {
                         const uint32_t fb = full_bar(s);
-                        const uint32_t sb = sbase + C::kOffB + s * C::kBBytes;
-                        const int kc = (tl.kb0 + kb) * 128;
                         mbar_arrive_expect_tx(fb, C::kBBytes);
                         if constexpr (kSwiGLU) {
                             // B as [2G halves][I rows][K]: one box of the tile's 128 gate rows
@@ -788,15 +809,40 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         armed |= 1u << s;
                         armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     }
-                    __syncwarp();
+                    if (++s == C::kStages) { s = 0; ph ^= 1u; }
                 }
-                // The MMA issuer copies a packed word to TMEM only at the tile's first K-group
-                // and at every fourth global K-group (one word holds four K-groups' scales):
-                // only those stages need their scale words.
+            }
+            if (aborted || *abort_flag) {
+                // Bounded drain of B loads that may still be landing in shared memory.
+                for (int i = 0; i < C::kStages; ++i)
+                    if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ----------------------------------------------------- scale loader
+        // Walks every stage with the producers.  A stage that starts a packed word row (the
+        // tile's first K-group and every fourth global K-group) receives the words of the
+        // tile's 128 A rows and BN B rows by 4-byte cp.async, written straight into the 32x4
+        // atom layout that tcgen05.cp reads (word (lane, j) of each atom holds MN index
+        // j * 32 + lane; rows outside the problem are zero-filled).  Each lane's arrival on
+        // every stage's full barrier fires when its copies have landed.
+        int s = 0;
+        uint32_t ph = 0;
+        TileIter<BN> it = tiles_of_cta<BN>(rank, split);
+        Tile tl;
+        bool aborted = false;
+        while (!aborted && it.next(p, total_tiles, sched, cnt, tl, p.kind == kContiguous)) {
+            const int32_t* pa0 = p.sfa + tl.sfa_g * p.sfa_gstride;
+            const int32_t* pb0 = p.sfb + tl.g * p.sfb_gstride;
+            for (int kb = 0; kb < tl.nkb; ++kb) {
+                // warp-uniform decision: every lane leaves together on abort
+                const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
+                if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 if (kb == 0 || ((tl.kb0 + kb) & 3) == 0) {
                     const int kw = (tl.kb0 + kb) >> 2;
                     const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
-                    const uint32_t da = sbase + C::kOffSfa + s * C::kSfaBytes + lane * 16;
+                    const uint32_t da = sbase + C::kOffSf + s * C::kSfSlotBytes + lane * 16;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int row = tl.sfa_row + lane + 32 * j;
@@ -804,7 +850,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         cp_async_4(da + 4 * j, in ? pa + row : pa, in ? 4u : 0u);
                     }
                     const int32_t* pb = pb0 + (long long)kw * p.sfb_ld;
-                    const uint32_t db = sbase + C::kOffSfb + s * C::kSfbBytes + lane * 16;
+                    const uint32_t db = da + C::kSfaBytes;
 #pragma unroll
                     for (int i = 0; i < C::kSfbAtoms; ++i) {
 #pragma unroll
@@ -821,27 +867,24 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             }
         }
         cp_async_wait_all();
-        if (!k2Sm && lane == 0 && (aborted || *abort_flag)) {
-            // Bounded drain of B loads that may still be landing in shared memory.
-            for (int i = 0; i < C::kStages; ++i)
-                if (armed >> i & 1u) drain_bar(full_bar(i), armed_par >> i & 1u, 20000000ull);
-        }
         __syncwarp();
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;                 // TMEM sub-partition this warp may read
-        const int ew = warp - 3;                // epilogue warp index (slot region)
-        const int row = q * 32 + lane;
+        const int row = q * 32 + lane;          // tile row of this thread (= threadIdx.x - kEpiThread0)
         const bool f32 = p.d_f32 != 0;
         const int cw = f32 ? 32 : 64;           // columns per chunk: 128 bytes per row
-        const uint32_t slot0 = sbase + C::kOffEpi + ew * C::kSlots * C::kSlotBytes;
-        uint8_t* slot0_ptr = smem + C::kOffEpi + ew * C::kSlots * C::kSlotBytes;
         const bool kg = p.kind == kKGrouped;
+        const int ew = warp - kEpiWarp0;        // epilogue warp index (slot region)
+        const uint32_t cslot0 = sbase + C::kOffCSlots + ew * C::kCSlots * C::kSlotBytes;
+        const uint8_t* cslot0_ptr = smem + C::kOffCSlots + ew * C::kCSlots * C::kSlotBytes;
+        const uint32_t dslot0 = sbase + C::kOffDSlots + ew * C::kDSlots * C::kSlotBytes;
+        uint8_t* dslot0_ptr = smem + C::kOffDSlots + ew * C::kDSlots * C::kSlotBytes;
 
         int acc = 0;
         uint32_t acc_ph = 0;
         bool aborted = false;
-        TileIter<BN> it = tiles_of_cta<BN, k2Sm>(rank, split);
+        TileIter<BN> it = tiles_of_cta<BN>(rank, split);
         Tile tl;
         if constexpr (kSplit) {
             // split-K: one tile per cluster, exchanged through distributed shared memory
@@ -856,121 +899,128 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 x_ph ^= 1u;
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
+        } else if constexpr (kSwiGLU) {
+            // ------------------------------------------ SwiGLU + per-1x128 requantisation
+            // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
+            // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
+            // codes into this warp's store slot (32 rows x 128 B, the TMA box) and a byte store of the scale into its packed word.  Two passes over
+            // TMEM: amax, then codes.
+            const uint32_t qslot = dslot0;
+            uint8_t* qslot_ptr = dslot0_ptr;
+            while (it.next(p, total_tiles, sched, cnt, tl)) {
+                const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+                if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
+                tc_fence_after();
+                const long long grow = tl.d_row + row;
+                bool row_ok = row < tl.valid_rows;
+                if (p.kind == kContiguous) {
+                    const int mi = __ldg(p.m_indices + grow);
+                    if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
+                    row_ok = (mi == tl.g);
+                }
+                const int nb = tl.n0 / 256;                      // 128-wide output column block
+                const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+                float amax = 0.0f;
+                if (tl.nkb > 0) {
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t g[32], u[32];
+                        tmem_ld_32x32b_x32(tacc + c0, g);
+                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
+                    }
+                }
+                const int e = scale_exponent(amax);
+                if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
+                __syncwarp();
+                uint8_t* rowp = qslot_ptr + lane * 128;
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t g[32], u[32];
+                    if (tl.nkb > 0) {
+                        tmem_ld_32x32b_x32(tacc + c0, g);
+                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
+                    }
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
+                        w[k] = word;
+                    }
+                    const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
+                    *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
+                if (row_ok) {
+                    const int sf_row = p.kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
+                    const int32_t* wp = p.sfq + (p.kind == kMasked ? tl.g * p.sfq_gstride : 0) +
+                                        (long long)(nb >> 2) * p.sfq_ld + sf_row;
+                    *(reinterpret_cast<uint8_t*>(const_cast<int32_t*>(wp)) + (nb & 3)) = static_cast<uint8_t>(e + 127);
+                }
+                // Dense rows past M are clipped by the TMA store; grouped layouts store only valid rows.
+                if (p.kind == kDense || __all_sync(0xffffffffu, row_ok)) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tm_d, qslot, nb * 128, tl.d_y + q * 32);
+                        bulk_commit_group();
+                    }
+                } else if (row_ok) {
+                    uint8_t* dst = static_cast<uint8_t*>(p.d) + grow * (p.N / 2) + nb * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(dst + 16 * j) = *reinterpret_cast<const uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                }
+                __syncwarp();
+                if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
+            }
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
         } else {
-            // C prefetch cursor (lane 0 issues): walks the same chunk sequence ahead.
-            TileIter<BN> cit = tiles_of_cta<BN, k2Sm>(rank, split);
+            // C prefetch cursor (lane 0): walks the same chunk sequence ahead, one 32-row x
+            // 32-column FP32 chunk per C slot, each refilled as soon as it has been read.
+            TileIter<BN> cit = tiles_of_cta<BN>(rank, split);
             Tile ctl;
-            bool c_have = (p.has_c && split == 1) ? cit.next(p, total_tiles, sched, cnt, ctl) : false;
+            bool c_have = false;
             int c_chunk = 0;
-            uint32_t c_issued = 0;       // chunks whose C load has been issued
-            auto issue_c = [&](uint32_t chunk_id) {
-                // chunk_id-th chunk of this warp's stream goes to slot chunk_id % kSlots
-                const int nch = (min(BN, p.N - ctl.n0) + 31) / 32;
-                const int sl = static_cast<int>(chunk_id % C::kSlots);
-                const uint32_t dst = slot0 + sl * C::kSlotBytes;
+            uint32_t c_issued = 0;       // C chunks whose load has been issued
+            auto issue_c = [&](uint32_t id) {
+                const int sl = static_cast<int>(id % C::kCSlots);
+                const uint32_t dst = cslot0 + sl * C::kSlotBytes;
                 const uint32_t bar = cfull_bar(ew, sl);
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, C::kSlotBytes);
                 const int x = ctl.n0 + c_chunk * 32;
                 if (kg) tma_load_3d(dst, &tm_c, bar, x, ctl.d_y + q * 32, ctl.d_z);
                 else tma_load_2d(dst, &tm_c, bar, x, ctl.d_y + q * 32);
-                if (++c_chunk == nch) {
+                if (++c_chunk == (min(BN, p.N - ctl.n0) + 31) / 32) {
                     c_chunk = 0;
                     c_have = cit.next(p, total_tiles, sched, cnt, ctl);
                 }
             };
-            if (lane == 0) {
-                while (c_have && c_issued + 1 < static_cast<uint32_t>(C::kSlots)) issue_c(c_issued++);
-            }
-
-            uint32_t chunk_id = 0;       // chunks consumed so far
-            if constexpr (kSwiGLU) {
-                // ------------------------------------------ SwiGLU + per-1x128 requantisation
-                // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
-                // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
-                // codes into this warp's slot (32 rows x 128 B, the TMA box) and a byte store of
-                // the scale into its packed word.  Two passes over TMEM: amax, then codes.
-                while (it.next(p, total_tiles, sched, cnt, tl)) {
-                    const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
-                    if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                    tc_fence_after();
-                    const long long grow = tl.d_row + row;
-                    bool row_ok = row < tl.valid_rows;
-                    if (p.kind == kContiguous) {
-                        const int mi = __ldg(p.m_indices + grow);
-                        if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
-                        row_ok = (mi == tl.g);
-                    }
-                    const int nb = tl.n0 / 256;                      // 128-wide output column block
-                    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-                    float amax = 0.0f;
-                    if (tl.nkb > 0) {
-                        for (int c0 = 0; c0 < 128; c0 += 32) {
-                            uint32_t g[32], u[32];
-                            tmem_ld_32x32b_x32(tacc + c0, g);
-                            tmem_ld_32x32b_x32(tacc + 128 + c0, u);
-                            tmem_wait_ld();
-    #pragma unroll
-                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
-                        }
-                    }
-                    const int e = scale_exponent(amax);
-                    if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
-                    __syncwarp();
-                    uint8_t* rowp = slot0_ptr + lane * 128;
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t g[32], u[32];
-                        if (tl.nkb > 0) {
-                            tmem_ld_32x32b_x32(tacc + c0, g);
-                            tmem_ld_32x32b_x32(tacc + 128 + c0, u);
-                            tmem_wait_ld();
-                        } else {
-    #pragma unroll
-                            for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
-                        }
-                        uint32_t w[8];
-    #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            uint32_t word = 0;
-    #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
-                            w[k] = word;
-                        }
-                        const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
-                        *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
-                    if (row_ok) {
-                        const int sf_row = p.kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
-                        const int32_t* wp = p.sfq + (p.kind == kMasked ? tl.g * p.sfq_gstride : 0) +
-                                            (long long)(nb >> 2) * p.sfq_ld + sf_row;
-                        *(reinterpret_cast<uint8_t*>(const_cast<int32_t*>(wp)) + (nb & 3)) = static_cast<uint8_t>(e + 127);
-                    }
-                    // Dense rows past M are clipped by the TMA store; grouped layouts store only valid rows.
-                    if (p.kind == kDense || __all_sync(0xffffffffu, row_ok)) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tm_d, slot0, nb * 128, tl.d_y + q * 32);
-                            bulk_commit_group();
-                        }
-                    } else if (row_ok) {
-                        uint8_t* dst = static_cast<uint8_t*>(p.d) + grow * (p.N / 2) + nb * 128;
-    #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            *reinterpret_cast<uint4*>(dst + 16 * j) = *reinterpret_cast<const uint4*>(rowp + ((j ^ (lane & 7)) << 4));
-                    }
-                    __syncwarp();
-                    if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
+            const bool load_c = p.has_c && !p.c_in_d;   // in place: the reduce-add brings C in
+            if constexpr (C::kCSlots > 0) {
+                if (lane == 0 && load_c) {
+                    c_have = cit.next(p, total_tiles, sched, cnt, ctl);
+                    while (c_have && c_issued < static_cast<uint32_t>(C::kCSlots)) issue_c(c_issued++);
                 }
             }
-            while (!kSwiGLU && it.next(p, total_tiles, sched, cnt, tl)) {
+
+            uint32_t chunk_id = 0;       // C chunks consumed so far
+            uint32_t dchunk = 0;         // chunks stored through the store slots
+            while (it.next(p, total_tiles, sched, cnt, tl)) {
                 // warp-uniform decision before the .sync.aligned TMEM loads below
-                const bool ok = wait_bar<k2Sm>(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
+                const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
                 const long long grow = tl.d_row + row;
@@ -985,11 +1035,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 const bool use_tma = (p.kind == kDense || kg) || __all_sync(0xffffffffu, row_ok);
                 const int ncols = min(BN, p.N - tl.n0);
                 const int nch = (ncols + cw - 1) / cw;
-                for (int ch = 0; ch < nch; ++ch, ++chunk_id) {
+                for (int ch = 0; ch < nch; ++ch) {
                     const int c0 = ch * cw;
-                    const int sl = static_cast<int>(chunk_id % C::kSlots);
-                    const uint32_t sl_addr = slot0 + sl * C::kSlotBytes;
-                    uint8_t* sl_ptr = slot0_ptr + sl * C::kSlotBytes;
                     uint32_t r[64];
                     if (tl.nkb > 0) {
                         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c0,
@@ -999,62 +1046,84 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                                                *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                         tmem_wait_ld();
                     } else {
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 64; ++i) r[i] = 0u;
                     }
                     if (!f32 && !(c0 + 32 < BN)) {
-    #pragma unroll
+#pragma unroll
                         for (int i = 32; i < 64; ++i) r[i] = 0u;
                     }
                     if (ch == nch - 1) {
                         // the accumulator buffer is free once its last columns are in registers
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) {
-                            if (k2Sm && !leader) mbar_arrive_remote(map_shared_rank(acce_bar(acc), 0));
-                            else mbar_arrive(acce_bar(acc));
-                        }
+                        if (lane == 0) mbar_arrive(acce_bar(acc));
                     }
                     // A 64-column BF16 chunk at the end of a BN = 224 tile would store into the
                     // neighbouring tile: such a chunk takes the per-thread path (no C in BF16).
                     if (use_tma && c0 + cw <= BN) {
-                        if (p.has_c) {
-                            if (lane == 0 && c_issued == chunk_id && c_have) {
-                                // not prefetched (single slot): load now, once the slot's last store is read
-                                bulk_wait_group_read<0>();
-                                issue_c(c_issued++);
+                        const int dsl = static_cast<int>(dchunk % C::kDSlots);
+                        const uint32_t d_addr = dslot0 + dsl * C::kSlotBytes;
+                        uint8_t* drow = dslot0_ptr + dsl * C::kSlotBytes + lane * 128;
+                        if (load_c) {       // FP32 chunks: add C
+                            const uint8_t* crow;
+                            if constexpr (C::kCSlots > 0) {
+                                const int csl = static_cast<int>(chunk_id % C::kCSlots);
+                                const bool okc = wait_bar(cfull_bar(ew, csl), (chunk_id / C::kCSlots) & 1u, wctl,
+                                                          kWaitEpilogueC);
+                                if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
+                                crow = cslot0_ptr + csl * C::kSlotBytes + lane * 128;
+                            } else {
+                                // no C slots (the widest tiles): this chunk's C lands in the store
+                                // slot once the store issued from it has read it, and D replaces
+                                // it in place
+                                if (lane == 1) bulk_wait_group_read<0>();
+                                __syncwarp();
+                                const uint32_t bar = dcfull_bar(ew, dsl);
+                                if (lane == 0) {
+                                    fence_proxy_async_smem();
+                                    mbar_arrive_expect_tx(bar, C::kSlotBytes);
+                                    if (kg) tma_load_3d(d_addr, &tm_c, bar, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
+                                    else tma_load_2d(d_addr, &tm_c, bar, tl.n0 + c0, tl.d_y + q * 32);
+                                }
+                                const bool okc = wait_bar(bar, (dchunk / C::kDSlots) & 1u, wctl, kWaitEpilogueC);
+                                if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
+                                crow = drow;
                             }
-                            __syncwarp();
-                            const bool okc = wait_bar(cfull_bar(ew, sl), (chunk_id / C::kSlots) & 1u, wctl, kWaitEpilogueC);
-                            if (!__all_sync(0xffffffffu, okc)) { aborted = true; break; }
-                        } else {
-                            // the slot's previous store (kSlots chunks ago) must have been read
-                            if (lane == 0) {
-                                if (C::kSlots == 1) bulk_wait_group_read<0>();
-                                else bulk_wait_group_read<C::kSlots - 1>();
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 cv = *reinterpret_cast<const float4*>(crow + ((j ^ (lane & 7)) << 4));
+                                r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + cv.x);
+                                r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + cv.y);
+                                r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + cv.z);
+                                r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + cv.w);
                             }
-                            __syncwarp();
+                            if constexpr (C::kCSlots > 0) {
+                                // the C slot is read: refill it with the chunk kCSlots ahead
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0 && c_have) issue_c(c_issued++);
+                                ++chunk_id;
+                            }
                         }
-                        uint8_t* rowp = sl_ptr + lane * 128;
-    #pragma unroll
+                        // the store slot's previous store (kDSlots chunks ago) must have read it
+                        if (lane == 1) {
+                            if constexpr (C::kDSlots == 1) bulk_wait_group_read<0>();
+                            else bulk_wait_group_read<C::kDSlots - 1>();
+                        }
+                        __syncwarp();
+#pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            uint4* cell = reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4));
+                            uint4* cell = reinterpret_cast<uint4*>(drow + ((j ^ (lane & 7)) << 4));
                             uint4 w;
                             if (f32) {
-                                float v0 = __uint_as_float(r[4 * j]), v1 = __uint_as_float(r[4 * j + 1]);
-                                float v2 = __uint_as_float(r[4 * j + 2]), v3 = __uint_as_float(r[4 * j + 3]);
-                                if (p.has_c) {
-                                    const float4 cv = *reinterpret_cast<const float4*>(cell);
-                                    v0 += cv.x; v1 += cv.y; v2 += cv.z; v3 += cv.w;
-                                }
-                                w = make_uint4(__float_as_uint(v0), __float_as_uint(v1), __float_as_uint(v2),
-                                               __float_as_uint(v3));
+                                w = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                             } else {
                                 uint32_t pk[4];
-    #pragma unroll
+#pragma unroll
                                 for (int i = 0; i < 4; ++i) {
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
-                                                                                    __uint_as_float(r[8 * j + 2 * i + 1]));
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                        __uint_as_float(r[8 * j + 2 * i]), __uint_as_float(r[8 * j + 2 * i + 1]));
                                     pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
                                 }
                                 w = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -1063,38 +1132,36 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
-                            if (kg) tma_store_3d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
-                            else tma_store_2d(&tm_d, sl_addr, tl.n0 + c0, tl.d_y + q * 32);
-                            bulk_commit_group();
-                            if (C::kSlots > 1 && p.has_c && c_have) {
-                                // refill the slot used by the previous chunk, once its store has read it
-                                bulk_wait_group_read<1>();
-                                issue_c(c_issued++);
+                        if (lane == 1) {
+                            if (p.c_in_d) {
+                                if (kg) tma_reduce_add_3d(&tm_d, d_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
+                                else tma_reduce_add_2d(&tm_d, d_addr, tl.n0 + c0, tl.d_y + q * 32);
+                            } else {
+                                if (kg) tma_store_3d(&tm_d, d_addr, tl.n0 + c0, tl.d_y + q * 32, tl.d_z);
+                                else tma_store_2d(&tm_d, d_addr, tl.n0 + c0, tl.d_y + q * 32);
                             }
+                            bulk_commit_group();
                         }
+                        ++dchunk;
                     } else {
                         // Partially valid row group (no C in these layouts) or a chunk reaching past
-                        // the tile: per-thread stores of the valid rows and columns.  Drain the slot
-                        // stores first so the slot accounting above stays conservative.
-                        if (lane == 0) bulk_wait_group_read<0>();
-                        __syncwarp();
+                        // the tile: per-thread stores of the valid rows and columns.
                         if (row_ok) {
                             const int left = ncols - c0;
                             if (f32) {
                                 float* dp = static_cast<float*>(p.d) + grow * p.N + tl.n0 + c0;
-    #pragma unroll
+#pragma unroll
                                 for (int j = 0; j < 8; ++j)
                                     if (4 * j < left)
                                         *reinterpret_cast<uint4*>(dp + 4 * j) =
                                             make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
                             } else {
                                 __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.d) + grow * p.N + tl.n0 + c0;
-    #pragma unroll
+#pragma unroll
                                 for (int j = 0; j < 8; ++j) {
                                     if (8 * j < left) {
                                         uint32_t pk[4];
-    #pragma unroll
+#pragma unroll
                                         for (int i = 0; i < 4; ++i) {
                                             const __nv_bfloat162 b2 = __floats2bfloat162_rn(
                                                 __uint_as_float(r[8 * j + 2 * i]), __uint_as_float(r[8 * j + 2 * i + 1]));
@@ -1110,26 +1177,25 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 if (aborted) break;
                 if (++acc == C::kNumAcc) { acc = 0; acc_ph ^= 1u; }
             }
-            if (lane == 0) {
+            if constexpr (C::kCSlots > 0) {
                 // C loads issued but never consumed (abort) must land before the CTA exits.
-                for (uint32_t c = chunk_id; c < c_issued; ++c)
-                    drain_bar(cfull_bar(ew, static_cast<int>(c % C::kSlots)), (c / C::kSlots) & 1u, 20000000ull);
-                bulk_wait_group_read<0>();   // the slots are read; the stores complete with the grid
+                if (lane == 0)
+                    for (uint32_t c = chunk_id; c < c_issued; ++c)
+                        drain_bar(cfull_bar(ew, static_cast<int>(c % C::kCSlots)), (c / C::kCSlots) & 1u, 20000000ull);
             }
+            if (lane == 1) bulk_wait_group_read<0>();   // the slots are read; the stores complete with the grid
             __syncwarp();
         }   // not split-K
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    // pair: the leader's MMAs may use this CTA's memory until here; split-K: peers read
-    // this CTA's exchange buffer until here
-    if (k2Sm || split > 1) cluster_sync();
+    // split-K: peers read this CTA's exchange buffer until here
+    if (split > 1) cluster_sync();
     else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        if constexpr (k2Sm) tmem_dealloc_pair(tmem_base, 512);
-        else tmem_dealloc(tmem_base, 512);
+        tmem_dealloc(tmem_base, 512);
     }
 }
 

@@ -8,11 +8,4 @@ template cudaError_t launch_gemm<128, kMajNT>(const GemmParams&, const GemmMaps&
 template cudaError_t launch_gemm<192, kMajNT>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
 template cudaError_t launch_gemm<224, kMajNT>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
 template cudaError_t launch_gemm<256, kMajNT>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
-// CTA-pair variants (dense)
-template cudaError_t launch_gemm<128, kMajNT, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
-template cudaError_t launch_gemm<224, kMajNT, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
-template cudaError_t launch_gemm<256, kMajNT, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
-template cudaError_t max_active_clusters<128, kMajNT, true>(int, int*);
-template cudaError_t max_active_clusters<224, kMajNT, true>(int, int*);
-template cudaError_t max_active_clusters<256, kMajNT, true>(int, int*);
 }  // namespace fg

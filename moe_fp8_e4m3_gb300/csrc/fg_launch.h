@@ -9,16 +9,15 @@
 
 namespace fg {
 
-// Launches fg_gemm_kernel<BN, kMaj, k2Sm, kSplit> with `grid` persistent CTAs on `stream`.
+// Launches fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU> with `grid` persistent CTAs on `stream`.
 // kMaj: operand majors (kMajNT, kMajNN, kMajTN, kMajTT).
-// k2Sm: clusters of two CTAs sharing one 256-row MMA (dense NT only).
 // kSplit: clusters of p.split CTAs sharing one tile along K (dense NT only).
 // kSwiGLU: BN = 256 tiles of 128 gate + 128 up columns, SwiGLU + FP8 requantisation epilogue.
-template <int BN, int kMaj, bool k2Sm = false, bool kSplit = false, bool kSwiGLU = false>
+template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false>
 cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream);
 
-// How many clusters of `cluster` CTAs of fg_gemm_kernel<BN, kMaj, k2Sm, kSplit> can be resident at once.
-template <int BN, int kMaj, bool k2Sm = false, bool kSplit = false, bool kSwiGLU = false>
+// How many clusters of `cluster` CTAs of fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU> can be resident at once.
+template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false>
 cudaError_t max_active_clusters(int cluster, int* out);
 
 }  // namespace fg

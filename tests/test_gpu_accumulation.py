@@ -7,8 +7,8 @@ block-scaled MMA applies the UE8M0 scales inside the tensor core and accumulates
 tensor memory over the whole K loop.  These tests check that reading at K = 16384 with
 per-group magnitudes spanning about +-20 binades, falling along K so that the smallest
 groups are added after the largest, in every launch form the dense GEMM can take (one
-CTA per tile, split-K clusters, CTA pairs), in the K-grouped GEMM with one expert owning
-all of K, and at the decode shape (M = 64)."""
+CTA per tile, split-K clusters), in the K-grouped GEMM with one expert owning all of K, and
+at the decode shape (M = 64)."""
 import numpy as np
 import pytest
 
@@ -45,7 +45,7 @@ def wide_dense_case(seed, m, n, k, with_c, out):
             "c": w["c"], "out": out}
 
 
-@pytest.mark.parametrize("form", ["default", "one_cta", "split4", "pairs"])
+@pytest.mark.parametrize("form", ["default", "one_cta", "split4"])
 @pytest.mark.parametrize("with_c,out", [(True, "f32"), (False, "f32"), (False, "bf16")])
 def test_dense_k16384_wide_range(fg, form, with_c, out, monkeypatch):
     from gpu_util import GuardedOut, dev
@@ -54,8 +54,6 @@ def test_dense_k16384_wide_range(fg, form, with_c, out, monkeypatch):
         monkeypatch.setenv("FG_FORCE_SPLIT", "1")
     elif form == "split4":
         monkeypatch.setenv("FG_FORCE_SPLIT", "4")
-    elif form == "pairs":
-        monkeypatch.setenv("FG_2SM", "1")
     case = wide_dense_case(4242, m, n, k, with_c, out)
     got = GuardedOut(m, n, out)
     c_t = dev(case["c"]) if with_c else None

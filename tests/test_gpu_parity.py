@@ -94,6 +94,18 @@ def test_dense_d_aliases_c(fg):
     C.compare(got.values(), C.dense_ref(case), "aliased C")
 
 
+@pytest.mark.parametrize("bn,split", [("224", "1"), ("256", "1"), ("128", "1"), ("128", "2")])
+def test_dense_in_place_every_form(fg, bn, split, monkeypatch):
+    """D aliasing C (in-place accumulation) in the one-CTA kernels, where the product is
+    added onto D by TMA reduce-adds (tile widths with and without C slots), and in a
+    split-K cluster, where each thread reads C and writes D."""
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    monkeypatch.setenv("FG_FORCE_SPLIT", split)
+    case = C.dense_case(811, 300, 528, 640, True, "f32")
+    got = run_dense(fg, case, alias_c=True)
+    C.compare(got.values(), C.dense_ref(case), f"in place BN={bn} split={split}")
+
+
 def test_scale_identification_probe_bit_exact(fg):
     """A = B = 1.0; every (row, group) and (n-block, group) scale is a distinct power of
     two, so each FP32 output names exactly which scales were applied."""
@@ -286,6 +298,20 @@ def run_k_grouped(fg, case, alias_c=False):
     return d
 
 
+@pytest.mark.parametrize("bn", ["128", "256"])
+def test_k_grouped_in_place_tile_widths(fg, bn, monkeypatch):
+    """K-grouped accumulation into C itself (TMA reduce-adds) at both tile widths, with an
+    empty segment (its D must stay exactly C)."""
+    monkeypatch.setenv("FG_FORCE_BN", bn)
+    case = C.k_grouped_case(812, num_groups=3, m=256, n=384, ks=[384, 0, 256])
+    d = run_k_grouped(fg, case, alias_c=True)
+    ref = C.k_grouped_ref(case)
+    vals = d.values().reshape(case["g"], case["m"], case["n"])
+    for e in range(case["g"]):
+        C.compare(vals[e], ref[e], f"k-grouped in place BN={bn} group {e}")
+    assert np.array_equal(vals[1].astype(np.float32), case["c"][1])
+
+
 @pytest.mark.parametrize("alias_c", [False, True])
 def test_k_grouped_parity(fg, alias_c):
     case = C.k_grouped_case(5, num_groups=4, m=256, n=384, ks=[200, 0, 128, 300])
@@ -317,36 +343,6 @@ def test_k_grouped_bad_segments_reported(fg):
     st, detail = fg.get_device_error()
     assert st == fg.FG_ERR_DEVICE_CONTRACT and detail == 0x104
     assert np.all(d.is_sentinel())
-
-
-# ------------------------------------------------------- CTA-pair (2-SM) path
-@pytest.mark.parametrize("bn", ["128", "224", "256"])
-def test_dense_cta_pairs(fg, bn, monkeypatch):
-    """The opt-in 2-SM MMA path (FG_2SM=1): one 256-row MMA per CTA pair, each CTA
-    holding half of B.  Odd number of 128-row blocks (the last pair is half empty),
-    ragged N, and C aliasing D."""
-    monkeypatch.setenv("FG_2SM", "1")
-    monkeypatch.setenv("FG_FORCE_BN", bn)
-    case = C.dense_case(61, 3 * 128 + 40, 800, 768, True, "f32")
-    C.compare(run_dense(fg, case).values(), C.dense_ref(case), f"pairs BN={bn}")
-    C.compare(run_dense(fg, case, alias_c=True).values(), C.dense_ref(case), f"pairs BN={bn} aliased")
-
-
-def test_scale_probe_cta_pairs(fg, monkeypatch):
-    from gpu_util import GuardedOut, dev
-    monkeypatch.setenv("FG_2SM", "1")
-    m, n, groups = 512, 448, 8
-    ea, eb = P.scale_probe_inputs(m, n, groups)
-    a = np.full((m, groups * 128), 0x38, np.uint8)
-    b = np.full((n, groups * 128), 0x38, np.uint8)
-    out = GuardedOut(m, n, "f32")
-    fg.fp8_gemm_nt(dev(a), dev(F.pack_ue8m0((ea + 127).astype(np.uint8))), dev(b),
-                   dev(F.pack_ue8m0((eb + 127).astype(np.uint8))), out.tensor)
-    _status_ok(fg)
-    want = np.zeros((m, n))
-    for gg in range(groups):
-        want += 2.0 ** (7 + ea[:, gg][:, None] + eb[np.arange(n) // 128, gg][None, :])
-    assert np.array_equal(out.values(), want)
 
 
 # ------------------------------------------------------------ split-K clusters
