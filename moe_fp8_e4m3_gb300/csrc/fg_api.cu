@@ -291,6 +291,9 @@ void fill_common(GemmParams& p, const DeviceState& st) {
     p.pdl = g_pdl;
 }
 
+// C is an array of its own (not D): launch the variant that prefetches it into slots.
+bool separate_c(const GemmParams& p) { return p.has_c && !p.c_in_d; }
+
 int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
     if (p.split > 1) {
@@ -307,12 +310,22 @@ int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cud
         }
         return FG_OK;
     }
-    switch (bn) {
-        case 64: e = fg::launch_gemm<64, fg::kMajNT>(p, gm, grid, s); break;
-        case 128: e = fg::launch_gemm<128, fg::kMajNT>(p, gm, grid, s); break;
-        case 192: e = fg::launch_gemm<192, fg::kMajNT>(p, gm, grid, s); break;
-        case 224: e = fg::launch_gemm<224, fg::kMajNT>(p, gm, grid, s); break;
-        default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
+    if (separate_c(p)) {
+        switch (bn) {
+            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
+        }
+    } else {
+        switch (bn) {
+            case 64: e = fg::launch_gemm<64, fg::kMajNT>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, fg::kMajNT>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, fg::kMajNT>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, fg::kMajNT>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
+        }
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -345,7 +358,16 @@ int launch_swiglu(const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStr
 // Variants with an MN-major operand (kMajTN, kMajNN, kMajTT): BN 128 or 256, and 224 for TT.
 int launch_mn(int maj, int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
-    if (maj == fg::kMajTN)
+    const bool sep = separate_c(p);
+    if (sep && bn == 128 && maj == fg::kMajTN)
+        e = fg::launch_gemm<128, fg::kMajTN, false, false, true>(p, gm, grid, s);
+    else if (sep && bn == 128 && maj == fg::kMajNN)
+        e = fg::launch_gemm<128, fg::kMajNN, false, false, true>(p, gm, grid, s);
+    else if (sep && bn == 128 && maj == fg::kMajTT)
+        e = fg::launch_gemm<128, fg::kMajTT, false, false, true>(p, gm, grid, s);
+    else if (sep && bn == 224 && maj == fg::kMajTT)
+        e = fg::launch_gemm<224, fg::kMajTT, false, false, true>(p, gm, grid, s);
+    else if (maj == fg::kMajTN)
         e = bn == 128 ? fg::launch_gemm<128, fg::kMajTN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajTN>(p, gm, grid, s);
     else if (maj == fg::kMajNN)
         e = bn == 128 ? fg::launch_gemm<128, fg::kMajNN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajNN>(p, gm, grid, s);

@@ -9,9 +9,9 @@
 namespace fg {
 
 // Raises the kernel's dynamic shared-memory limit once per device.
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC>
 cudaError_t configure_gemm() {
-    constexpr int kSmem = TileCfg<BN, kSplit, kSwiGLU>::kSmemBytes;
+    constexpr int kSmem = TileCfg<BN, kSplit, kSwiGLU, kSepC>::kSmemBytes;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -20,7 +20,7 @@ cudaError_t configure_gemm() {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        err = cudaFuncSetAttribute(fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        err = cudaFuncSetAttribute(fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
         configured[dev] = true;
     }
@@ -47,31 +47,31 @@ inline void set_launch_attrs(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr,
     cfg.numAttrs = n;
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC>
 cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream) {
-    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU>();
+    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = TileCfg<BN, kSplit, kSwiGLU>::kSmemBytes;
+    cfg.dynamicSmemBytes = TileCfg<BN, kSplit, kSwiGLU, kSepC>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, kSplit ? p.split : 1, p.pdl != 0);
-    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU>, p, maps);
+    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC>, p, maps);
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC>
 cudaError_t max_active_clusters(int cluster, int* out) {
-    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU>();
+    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = TileCfg<BN, kSplit, kSwiGLU>::kSmemBytes;
+    cfg.dynamicSmemBytes = TileCfg<BN, kSplit, kSwiGLU, kSepC>::kSmemBytes;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, cluster, false);
-    return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC>, &cfg);
 }
 
 }  // namespace fg

@@ -131,7 +131,7 @@ struct GemmParams {
     int debug_stall;
 };
 
-template <int BN, bool kSplit = false, bool kSwiGLU = false>
+template <int BN, bool kSplit = false, bool kSwiGLU = false, bool kSepC = false>
 struct TileCfg {
     static constexpr int kBM = 128, kBK = 128;
     static constexpr int kSfbAtoms = (BN + 127) / 128;
@@ -150,19 +150,26 @@ struct TileCfg {
     static constexpr int kSfSlotBytes = kSfaBytes + kSfbBytes;
     // Epilogue, per warp: kCSlots slots where C chunks land (refilled as soon as read) and
     // kDSlots slots from which D chunks are stored; each slot is 32 rows x 128 bytes (one
-    // chunk: 32 FP32 or 64 BF16 columns).  Split-K variants exchange through the operand
-    // ring and use no slots; the SwiGLU variant stages one chunk of codes; tiles too wide
-    // for two accumulators rarely take C and give the space to pipeline stages (their C,
-    // if any, lands in the store slot).
+    // chunk: 32 FP32 or 64 BF16 columns).  Only the kSepC variants, launched when C is an
+    // array of its own, have C slots: without C, or with D aliasing C (accumulated by a TMA
+    // reduce-add), the space goes to pipeline stages.  Split-K variants exchange through
+    // the operand ring and use no slots; the SwiGLU variant stages one chunk of codes; tiles
+    // too wide for two accumulators give the space to stages even with a separate C (it
+    // then lands in the store slot).
     // (measured on GB300: the mainloop of these kernels is bound by the bytes its ring holds
-    // in flight, so narrow tiles give the space to a fifth stage)
-    static constexpr int kCSlots = (kSplit || kSwiGLU) ? 0 : (BN >= 256 ? 0 : (BN >= 192 ? 3 : 2));
-    static constexpr int kDSlots = kSplit ? 0 : 1;
+    // in flight, so every stage that fits counts)
+    // The stages are sized with one store slot per warp; a second one (the store of one chunk
+    // overlapping the next chunk's work) is added where the space left over holds it.
+    static constexpr int kCSlots = (!kSepC || kSplit || kSwiGLU) ? 0 : (BN >= 256 ? 0 : (BN >= 192 ? 3 : 2));
     static constexpr int kSlotBytes = 4096;
-    static constexpr int kEpiBytes = 4 * (kCSlots + kDSlots) * kSlotBytes;
+    static constexpr int kDSlotsMin = kSplit ? 0 : 1;
+    static constexpr int kEpiMin = 4 * (kCSlots + kDSlotsMin) * kSlotBytes;
     static constexpr int kMiscBytes = 1024 + 2 * (kMaxGroups + 1) * 4;   // barriers etc. + group tables
-    static constexpr int kStages0 = (kSmemLimit - 1024 - kEpiBytes - kMiscBytes) / (kStageBytes + kSfSlotBytes);
+    static constexpr int kStages0 = (kSmemLimit - 1024 - kEpiMin - kMiscBytes) / (kStageBytes + kSfSlotBytes);
     static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+    static constexpr int kSpare = kSmemLimit - 1024 - kEpiMin - kMiscBytes - kStages * (kStageBytes + kSfSlotBytes);
+    static constexpr int kDSlots = (kSplit || kSwiGLU) ? kDSlotsMin : (kSpare >= 4 * kSlotBytes ? 2 : 1);
+    static constexpr int kEpiBytes = 4 * (kCSlots + kDSlots) * kSlotBytes;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffEpi = kOffB + kStages * kBBytes;                 // 1024-aligned
@@ -495,7 +502,7 @@ __device__ __forceinline__ float swiglu_value(uint32_t gate, uint32_t up) {
     return __fdividef(x, 1.0f + __expf(-x)) * __uint_as_float(up);
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_a = maps.a;
@@ -507,7 +514,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
     static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
-    using C = TileCfg<BN, kSplit, kSwiGLU>;
+    static_assert(!kSepC || (!kSplit && !kSwiGLU), "C slots belong to the plain epilogue");
+    using C = TileCfg<BN, kSplit, kSwiGLU, kSepC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
