@@ -55,7 +55,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_split.cu",
-                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_sepc.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh", "fg_mqa.cu"]
+                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_sepc.cu", "fg_gemm_dense.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh", "fg_mqa.cu"]
 
 
 def align4(x: int) -> int:

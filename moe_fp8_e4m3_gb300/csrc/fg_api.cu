@@ -311,13 +311,21 @@ int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cud
         }
         return FG_OK;
     }
-    if (separate_c(p)) {
+    if (separate_c(p)) {   // dense (the grouped NT layouts take no C)
         switch (bn) {
-            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, true>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
+            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
+        }
+    } else if (p.kind == fg::kDense) {
+        switch (bn) {
+            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
+            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
+            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
+            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
+            default: e = fg::launch_gemm<256, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
         }
     } else {
         switch (bn) {
