@@ -114,11 +114,11 @@ int resident_clusters(DeviceState& st, int bn, int cluster) {
     int n = 0;
     cudaError_t e = cudaErrorInvalidValue;
     switch (bn) {
-        case 64: e = fg::max_active_clusters<64, fg::kMajNT, true>(cluster, &n); break;
-        case 128: e = fg::max_active_clusters<128, fg::kMajNT, true>(cluster, &n); break;
-        case 192: e = fg::max_active_clusters<192, fg::kMajNT, true>(cluster, &n); break;
-        case 224: e = fg::max_active_clusters<224, fg::kMajNT, true>(cluster, &n); break;
-        default: e = fg::max_active_clusters<256, fg::kMajNT, true>(cluster, &n); break;
+        case 64: e = fg::max_active_clusters<64, fg::kMajNT, true, false, false, fg::kDense>(cluster, &n); break;
+        case 128: e = fg::max_active_clusters<128, fg::kMajNT, true, false, false, fg::kDense>(cluster, &n); break;
+        case 192: e = fg::max_active_clusters<192, fg::kMajNT, true, false, false, fg::kDense>(cluster, &n); break;
+        case 224: e = fg::max_active_clusters<224, fg::kMajNT, true, false, false, fg::kDense>(cluster, &n); break;
+        default: e = fg::max_active_clusters<256, fg::kMajNT, true, false, false, fg::kDense>(cluster, &n); break;
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -295,47 +295,26 @@ void fill_common(GemmParams& p, const DeviceState& st) {
 // C is an array of its own (not D): launch the variant that prefetches it into slots.
 bool separate_c(const GemmParams& p) { return p.has_c && !p.c_in_d; }
 
+// One NT launch of the variant family <kSplit, kSepC, kKind> at tile width bn (BN=256 has no
+// C slots: its separate-C calls take the plain variant, C landing in the store slot).
+template <bool kSplit, bool kSepC, int kKind>
+cudaError_t launch_nt_bn(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    switch (bn) {
+        case 64: return fg::launch_gemm<64, fg::kMajNT, kSplit, false, kSepC, kKind>(p, gm, grid, s);
+        case 128: return fg::launch_gemm<128, fg::kMajNT, kSplit, false, kSepC, kKind>(p, gm, grid, s);
+        case 192: return fg::launch_gemm<192, fg::kMajNT, kSplit, false, kSepC, kKind>(p, gm, grid, s);
+        case 224: return fg::launch_gemm<224, fg::kMajNT, kSplit, false, kSepC, kKind>(p, gm, grid, s);
+        default: return fg::launch_gemm<256, fg::kMajNT, kSplit, false, false, kKind>(p, gm, grid, s);
+    }
+}
+
 int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
-    if (p.split > 1) {
-        switch (bn) {
-            case 64: e = fg::launch_gemm<64, fg::kMajNT, true>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, fg::kMajNT, true>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, fg::kMajNT, true>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, fg::kMajNT, true>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, fg::kMajNT, true>(p, gm, grid, s); break;
-        }
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return FG_ERR_CUDA;
-        }
-        return FG_OK;
-    }
-    if (separate_c(p)) {   // dense (the grouped NT layouts take no C)
-        switch (bn) {
-            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, true, true>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-        }
-    } else if (p.kind == fg::kDense) {
-        switch (bn) {
-            case 64: e = fg::launch_gemm<64, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, fg::kMajNT, false, false, false, true>(p, gm, grid, s); break;
-        }
-    } else {
-        switch (bn) {
-            case 64: e = fg::launch_gemm<64, fg::kMajNT>(p, gm, grid, s); break;
-            case 128: e = fg::launch_gemm<128, fg::kMajNT>(p, gm, grid, s); break;
-            case 192: e = fg::launch_gemm<192, fg::kMajNT>(p, gm, grid, s); break;
-            case 224: e = fg::launch_gemm<224, fg::kMajNT>(p, gm, grid, s); break;
-            default: e = fg::launch_gemm<256, fg::kMajNT>(p, gm, grid, s); break;
-        }
-    }
+    if (p.split > 1) e = launch_nt_bn<true, false, fg::kDense>(bn, p, gm, grid, s);
+    else if (p.kind == fg::kContiguous) e = launch_nt_bn<false, false, fg::kContiguous>(bn, p, gm, grid, s);
+    else if (p.kind == fg::kMasked) e = launch_nt_bn<false, false, fg::kMasked>(bn, p, gm, grid, s);
+    else if (separate_c(p)) e = launch_nt_bn<false, true, fg::kDense>(bn, p, gm, grid, s);
+    else e = launch_nt_bn<false, false, fg::kDense>(bn, p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -356,7 +335,9 @@ bool encode_swiglu_b(CUtensorMap* map, const void* b, int K, int I, int G) {
 }
 
 int launch_swiglu(const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
-    const cudaError_t e = fg::launch_gemm<256, fg::kMajNT, false, true>(p, gm, grid, s);
+    const cudaError_t e = p.kind == fg::kMasked
+                              ? fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kMasked>(p, gm, grid, s)
+                              : fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kContiguous>(p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -364,26 +345,38 @@ int launch_swiglu(const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStr
     return FG_OK;
 }
 
-// Variants with an MN-major operand (kMajTN, kMajNN, kMajTT): BN 128 or 256, and 224 for TT.
+// One launch with an MN-major operand at tile width bn (128 or 256; 224 as well for TT) of
+// layout kKind; a separate C takes the variant with C slots where the width has them (128,
+// and 224 for TT).
+template <int kMaj, int kKind>
+cudaError_t launch_mn_bn(int bn, bool sep, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    if (bn == 128) {
+        if (sep) return fg::launch_gemm<128, kMaj, false, false, true, kKind>(p, gm, grid, s);
+        return fg::launch_gemm<128, kMaj, false, false, false, kKind>(p, gm, grid, s);
+    }
+    if constexpr (kMaj == fg::kMajTT) {
+        if (bn == 224) {
+            if (sep) return fg::launch_gemm<224, kMaj, false, false, true, kKind>(p, gm, grid, s);
+            return fg::launch_gemm<224, kMaj, false, false, false, kKind>(p, gm, grid, s);
+        }
+    }
+    return fg::launch_gemm<256, kMaj, false, false, false, kKind>(p, gm, grid, s);
+}
+
+// Variants with an MN-major operand: dense TN / NN / TT, the K-grouped TN GEMM and the
+// M-grouped contiguous NN GEMM (the grouped layouts take no separate C except K-grouped).
 int launch_mn(int maj, int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
     cudaError_t e;
     const bool sep = separate_c(p);
-    if (sep && bn == 128 && maj == fg::kMajTN)
-        e = fg::launch_gemm<128, fg::kMajTN, false, false, true>(p, gm, grid, s);
-    else if (sep && bn == 128 && maj == fg::kMajNN)
-        e = fg::launch_gemm<128, fg::kMajNN, false, false, true>(p, gm, grid, s);
-    else if (sep && bn == 128 && maj == fg::kMajTT)
-        e = fg::launch_gemm<128, fg::kMajTT, false, false, true>(p, gm, grid, s);
-    else if (sep && bn == 224 && maj == fg::kMajTT)
-        e = fg::launch_gemm<224, fg::kMajTT, false, false, true>(p, gm, grid, s);
-    else if (maj == fg::kMajTN)
-        e = bn == 128 ? fg::launch_gemm<128, fg::kMajTN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajTN>(p, gm, grid, s);
+    const bool dense = p.kind == fg::kDense;
+    if (maj == fg::kMajTN)
+        e = dense ? launch_mn_bn<fg::kMajTN, fg::kDense>(bn, sep, p, gm, grid, s)
+                  : launch_mn_bn<fg::kMajTN, fg::kKGrouped>(bn, sep, p, gm, grid, s);
     else if (maj == fg::kMajNN)
-        e = bn == 128 ? fg::launch_gemm<128, fg::kMajNN>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajNN>(p, gm, grid, s);
-    else if (bn == 224)
-        e = fg::launch_gemm<224, fg::kMajTT>(p, gm, grid, s);
+        e = dense ? launch_mn_bn<fg::kMajNN, fg::kDense>(bn, sep, p, gm, grid, s)
+                  : launch_mn_bn<fg::kMajNN, fg::kContiguous>(bn, false, p, gm, grid, s);
     else
-        e = bn == 128 ? fg::launch_gemm<128, fg::kMajTT>(p, gm, grid, s) : fg::launch_gemm<256, fg::kMajTT>(p, gm, grid, s);
+        e = launch_mn_bn<fg::kMajTT, fg::kDense>(bn, sep, p, gm, grid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;

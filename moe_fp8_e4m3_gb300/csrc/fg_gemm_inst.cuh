@@ -9,7 +9,7 @@
 namespace fg {
 
 // Raises the kernel's dynamic shared-memory limit once per device.
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, bool kDenseT>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, int kKindT>
 cudaError_t configure_gemm() {
     constexpr int kSmem = TileCfg<BN, kSplit, kSwiGLU, kSepC>::kSmemBytes;
     int dev = 0;
@@ -20,7 +20,7 @@ cudaError_t configure_gemm() {
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        err = cudaFuncSetAttribute(fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        err = cudaFuncSetAttribute(fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
         configured[dev] = true;
     }
@@ -47,9 +47,9 @@ inline void set_launch_attrs(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr,
     cfg.numAttrs = n;
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, bool kDenseT>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, int kKindT>
 cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream) {
-    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT>();
+    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -58,12 +58,12 @@ cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cud
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, kSplit ? p.split : 1, p.pdl != 0);
-    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT>, p, maps);
+    return cudaLaunchKernelEx(&cfg, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT>, p, maps);
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, bool kDenseT>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, int kKindT>
 cudaError_t max_active_clusters(int cluster, int* out) {
-    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT>();
+    cudaError_t err = configure_gemm<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cluster));
@@ -71,7 +71,7 @@ cudaError_t max_active_clusters(int cluster, int* out) {
     cfg.dynamicSmemBytes = TileCfg<BN, kSplit, kSwiGLU, kSepC>::kSmemBytes;
     cudaLaunchAttribute attr[2];
     set_launch_attrs(cfg, attr, cluster, false);
-    return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT>, &cfg);
 }
 
 }  // namespace fg

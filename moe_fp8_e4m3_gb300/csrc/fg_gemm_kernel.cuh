@@ -504,7 +504,7 @@ __device__ __forceinline__ float swiglu_value(uint32_t gate, uint32_t up) {
     return __fdividef(x, 1.0f + __expf(-x)) * __uint_as_float(up);
 }
 
-template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, bool kDenseT>
+template <int BN, int kMaj, bool kSplit, bool kSwiGLU, bool kSepC, int kKindT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_a = maps.a;
@@ -517,7 +517,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
     static_assert(!kSepC || (!kSplit && !kSwiGLU), "C slots belong to the plain epilogue");
-    static_assert(!kDenseT || !kSwiGLU, "the SwiGLU epilogue is a grouped layout");
+    static_assert(!kSwiGLU || kKindT == kContiguous || kKindT == kMasked, "the SwiGLU epilogue is an M-grouped layout");
+    static_assert(!kSplit || kKindT == kDense, "split-K clusters are dense");
     using C = TileCfg<BN, kSplit, kSwiGLU, kSepC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -525,11 +526,11 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Split-K cluster: rank r runs the r-th share of the K-groups.
     const int split = kSplit ? p.split : 1;   // a compile-time 1 outside the split-K variant
-    // The dense-only variants (and split-K clusters, dense by construction) fix the layout at
-    // compile time: their code holds the dense tile walk alone, so less of it has to be
-    // fetched cold when the kernel starts (measured on GB300: the decode GEMM behind the
-    // prefill 21.9 -> 19.8 us).
-    const int kind = (kSplit || kDenseT) ? static_cast<int>(kDense) : p.kind;
+    // The layout is fixed at compile time (kKindT; -1 reads it from the call): each variant's
+    // code holds one tile walk, so less of it has to be fetched cold when the kernel starts
+    // (measured on GB300: the decode GEMM behind the prefill 21.9 -> 19.8 us, the prefill
+    // 75.2 -> 72.7 us).
+    const int kind = kKindT >= 0 ? kKindT : p.kind;
     const int rank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
 
     const uint32_t bar0 = sbase + C::kOffBar;

@@ -4,5 +4,6 @@
 #include "fg_gemm_inst.cuh"
 
 namespace fg {
-template cudaError_t launch_gemm<256, kMajNT, false, true>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, kMajNT, false, true, false, kContiguous>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
+template cudaError_t launch_gemm<256, kMajNT, false, true, false, kMasked>(const GemmParams&, const GemmMaps&, int, cudaStream_t);
 }  // namespace fg

@@ -9,17 +9,17 @@
 
 namespace fg {
 
-// Launches fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT> with `grid` persistent CTAs on `stream`.
+// Launches fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT> with `grid` persistent CTAs on `stream`.
 // kMaj: operand majors (kMajNT, kMajNN, kMajTN, kMajTT).
 // kSplit: clusters of p.split CTAs sharing one tile along K (dense NT only).
 // kSwiGLU: BN = 256 tiles of 128 gate + 128 up columns, SwiGLU + FP8 requantisation epilogue.
 // kSepC: shared-memory slots that prefetch C, for a C that is not D (fewer pipeline stages).
-// kDenseT: dense calls only (the layout is fixed at compile time).
-template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false, bool kSepC = false, bool kDenseT = false>
+// kKindT: the layout (GemmKind) the variant serves, fixed at compile time (-1: read from p.kind).
+template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false, bool kSepC = false, int kKindT = -1>
 cudaError_t launch_gemm(const GemmParams& p, const GemmMaps& maps, int grid, cudaStream_t stream);
 
-// How many clusters of `cluster` CTAs of fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kDenseT> can be resident at once.
-template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false, bool kSepC = false, bool kDenseT = false>
+// How many clusters of `cluster` CTAs of fg_gemm_kernel<BN, kMaj, kSplit, kSwiGLU, kSepC, kKindT> can be resident at once.
+template <int BN, int kMaj, bool kSplit = false, bool kSwiGLU = false, bool kSepC = false, int kKindT = -1>
 cudaError_t max_active_clusters(int cluster, int* out);
 
 }  // namespace fg
