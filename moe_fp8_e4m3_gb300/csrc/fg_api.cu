@@ -202,24 +202,23 @@ int forced_split() {
 
 // N-tile choice.  Cost model: the busiest SM runs ceil(tiles / SMs) tiles, each costing
 // about (BN + 32) column units (the 32 stands for the A re-read and fixed per-tile work).
-// With a heavy epilogue (a C, or an FP32 D: 4 bytes per output) only double-buffered tile
-// widths (BN <= 224) are considered, so the epilogue of one tile overlaps the MMAs of the
-// next (measured on GB300, 4096 x 7168 x 2048 FP32 D without C: BN=224 67 us, BN=256 74 us).
+// BN=256 has a single TMEM accumulator, so its epilogue does not overlap the next tile's
+// MMAs: it is charged 15 % more, and with a heavy epilogue (a C, or an FP32 D: 4 bytes per
+// output) it is not considered.  Measured on GB300: 4096 x 7168 x 2048 FP32 D without C,
+// BN=224 67 us against BN=256 74 us; BF16 D, masked 32 x 256 x 4096 x 2048 62.1 us against
+// 63.9 us and contiguous 32 x 4096 x 4096 137.9 us against 140.2 us.
 int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue) {
     const int f = forced_bn();
     if (f == 64 || f == 128 || f == 192 || f == 224 || f == 256) return f;
     int best = 128;
-    long long best_cost = -1, best_waves = 0;
-    for (int bn : {256, 224, 192, 128, 64}) {
+    double best_cost = -1.0;
+    for (int bn : {224, 256, 192, 128, 64}) {
         if (heavy_epilogue && bn == 256) continue;
         const long long tiles = row_blocks * ceil_div(n, bn);
         const long long waves = (tiles + sms - 1) / sms;
-        const long long cost = waves * (bn + 32);
-        if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; best_waves = waves; }
+        const double cost = static_cast<double>(waves * (bn + 32)) * (bn == 256 ? 1.15 : 1.0);
+        if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
     }
-    // Without C the widest tile reads A fewest times; measured on GB300 it wins whenever it
-    // needs no more waves (masked 32 x 256 x 4096 x 2048: 71 us against 74 us at BN=224).
-    if (!heavy_epilogue && best != 256 && (row_blocks * ceil_div(n, 256) + sms - 1) / sms <= best_waves) best = 256;
     return best;
 }
 
