@@ -237,7 +237,10 @@ double t_kb_us(int bn) {
         default: return 0.61;
     }
 }
-double t_x_us(int s) { return s <= 1 ? 0.0 : (s == 2 ? 0.5 : (s == 4 ? 2.5 : 5.0)); }
+// t_x: the split-K epilogue (partials through distributed shared memory, cluster barriers)
+// over a plain one; per-CTA timelines on GB300 put the 2-CTA exchange at ~3.6 us against
+// ~1 us (and 128x256x512 runs in 8.6 us unsplit against 11.6 us in 2-CTA clusters).
+double t_x_us(int s) { return s <= 1 ? 0.0 : (s == 2 ? 2.5 : (s == 4 ? 4.0 : 6.0)); }
 
 struct DenseTiling {
     int bn;
