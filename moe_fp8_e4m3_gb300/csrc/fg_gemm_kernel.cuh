@@ -920,8 +920,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             // ------------------------------------------ SwiGLU + per-1x128 requantisation
             // Per tile and row: y[i] = SiLU(gate[i]) * up[i] for the tile's 128 outputs
             // (TMEM columns i and 128 + i), one UE8M0 scale for the row's 128 values, E4M3
-            // codes into this warp's store slot (32 rows x 128 B, the TMA box) and a byte store of the scale into its packed word.  Two passes over
-            // TMEM: amax, then codes.
+            // codes into this warp's store slot (32 rows x 128 B, the TMA box) and a byte
+            // store of the scale into its packed word.  One pass over TMEM keeps the row's 128
+            // values in registers, so the single accumulator is free for the next tile's
+            // MMAs before the codes are formed.
             const uint32_t qslot = dslot0;
             uint8_t* qslot_ptr = dslot0_ptr;
             while (it.next(p, total_tiles, sched, cnt, tl)) {
@@ -937,47 +939,46 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 }
                 const int nb = tl.n0 / 256;                      // 128-wide output column block
                 const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+                float y[128];
                 float amax = 0.0f;
-                if (tl.nkb > 0) {
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t g[32], u[32];
-                        tmem_ld_32x32b_x32(tacc + c0, g);
-                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
-                        tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(swiglu_value(g[i], u[i])));
+                for (int c0 = 0; c0 < 128; c0 += 16) {
+                    uint32_t g[16], u[16];
+                    if (tl.nkb > 0) {
+                        tmem_ld_32x32b_x16(tacc + c0, g);
+                        tmem_ld_32x32b_x16(tacc + 128 + c0, u);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) g[i] = u[i] = 0u;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        y[c0 + i] = swiglu_value(g[i], u[i]);
+                        amax = fmaxf(amax, fabsf(y[c0 + i]));
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
                 const int e = scale_exponent(amax);
                 if (lane == 0) bulk_wait_group_read<0>();    // the slot's previous store has read it
                 __syncwarp();
                 uint8_t* rowp = qslot_ptr + lane * 128;
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t g[32], u[32];
-                    if (tl.nkb > 0) {
-                        tmem_ld_32x32b_x32(tacc + c0, g);
-                        tmem_ld_32x32b_x32(tacc + 128 + c0, u);
-                        tmem_wait_ld();
-                    } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) g[i] = u[i] = 0u;
-                    }
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t w[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         uint32_t word = 0;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            word |= e4m3(ldexpf(swiglu_value(g[4 * k + j], u[4 * k + j]), -e)) << (8 * j);
+                        for (int j = 0; j < 4; ++j) word |= e4m3(ldexpf(y[c0 + 4 * k + j], -e)) << (8 * j);
                         w[k] = word;
                     }
                     const int cell = (c0 / 32) * 2;               // 32 codes = two 16-byte cells
                     *reinterpret_cast<uint4*>(rowp + ((cell ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4*>(rowp + (((cell + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acce_bar(acc));        // the accumulator is free
                 if (row_ok) {
                     const int sf_row = kind == kMasked ? tl.sfa_row + row : static_cast<int>(grow);
                     const int32_t* wp = p.sfq + (kind == kMasked ? tl.g * p.sfq_gstride : 0) +
