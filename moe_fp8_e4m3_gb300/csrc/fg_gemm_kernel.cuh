@@ -1037,14 +1037,16 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             uint32_t chunk_id = 0;       // C chunks consumed so far
             uint32_t dchunk = 0;         // chunks stored through the store slots
             while (it.next(p, total_tiles, sched, cnt, tl)) {
+                // the row's expert id is loaded before the accumulator wait (its latency
+                // overlaps the wait instead of following it)
+                const long long grow = tl.d_row + row;
+                const int mi = kind == kContiguous ? __ldg(p.m_indices + grow) : 0;
                 // warp-uniform decision before the .sync.aligned TMEM loads below
                 const bool ok = wait_bar(accf_bar(acc), acc_ph, wctl, kWaitEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
                 tc_fence_after();
-                const long long grow = tl.d_row + row;
                 bool row_ok = row < tl.valid_rows;
                 if (kind == kContiguous) {
-                    const int mi = __ldg(p.m_indices + grow);
                     if (mi >= 0 && mi != tl.g) record_status(p.status, kErrContract | kChkMixedBlock);
                     row_ok = (mi == tl.g);
                 }
