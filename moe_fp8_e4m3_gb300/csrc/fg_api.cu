@@ -776,6 +776,7 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total, const 
     p.M = M; p.N = N; p.K = K_total; p.G = G;
     p.d_f32 = 1; p.has_c = c != nullptr;
     p.c_in_d = c != nullptr && c == d;
+    p.c = c;
     p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
     p.sfa_ld = align4(M); p.sfb_ld = align4(N);
