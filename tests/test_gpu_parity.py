@@ -65,7 +65,7 @@ def test_dense_every_tile_width(fg, bn, out, monkeypatch):
     C.compare(got.values(), C.dense_ref(case), f"BN={bn} {out}")
 
 
-@pytest.mark.parametrize("bn", ["64", "192", "224", "256"])
+@pytest.mark.parametrize("bn", ["64", "128", "192", "224", "256"])
 def test_grouped_every_tile_width(fg, bn, monkeypatch):
     monkeypatch.setenv("FG_FORCE_BN", bn)
     case = C.contiguous_case(9, num_tokens=512, num_routed=16, topk=3, num_groups=5, n=448, k=256)
