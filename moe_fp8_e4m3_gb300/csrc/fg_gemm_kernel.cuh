@@ -31,18 +31,22 @@
 //               issuer waits once per stage for operands and scales, and this warp never
 //               waits for load latency
 //   warps 4..7  epilogue: TMEM -> registers, + C -> BF16/FP32 -> TMA store, each warp on
-//               its own 32 rows: C chunks land in slots of their own, loaded ahead by lane 0
-//               and refilled as soon as read; D chunks leave from store slots through TMA
-//               stores issued by lane 1 (the two TMA streams of a warp proceed side by side).
-//               When D is C itself (in-place accumulation) no C is loaded: the accumulator
-//               chunk leaves through a TMA reduce-add, and L2 adds it onto D.
-// The MMA issuer is the throughput limit of narrow tiles (measured on GB300: ~55 clocks to
-// issue one tcgen05.mma and ~200 to test an mbarrier, against 448 clocks of tensor work per
-// 128 x 224 x 128 K-group), so its loop is lean: descriptors are precomputed per stage, and
-// when the next two stages have both landed (two pipelined non-blocking tests) it issues
-// both stages' MMAs after one round of waiting.
+//               its own 32 rows.  A C that is an array of its own (the kSepC variants) lands
+//               in C slots, loaded ahead by lane 0 and refilled as soon as read; D chunks
+//               leave from store slots through TMA stores issued by lane 1 (the two TMA
+//               streams of a warp proceed side by side).  When D is C itself (in-place
+//               accumulation) no C is loaded: the accumulator chunk leaves through a TMA
+//               reduce-add, and L2 adds it onto D.
+// The MMA issuer's loop is lean (measured on GB300: ~55 clocks to issue one tcgen05.mma and
+// ~200 to test an mbarrier, against 448 clocks of tensor work per 128 x 224 x 128 K-group):
+// descriptors are precomputed per stage, and when the next two stages have both landed (two
+// pipelined non-blocking tests) it issues both stages' MMAs after one round of waiting.
+// The mainloop's pace is the ring's round trip (load latency + MMA issue and execution)
+// over its stage count, so shared memory goes to stages first.
 // Accumulators are double-buffered in TMEM when two fit next to the scale slots
 // (BN <= 224), so the epilogue of one tile overlaps the MMAs of the next.
+// Each variant serves one layout (dense, contiguous, masked, K-grouped), fixed at compile
+// time, so a launch fetches one tile walk's code.
 //
 // Split-K clusters (dense NT, few output tiles): a cluster of `split` CTAs shares one
 // output tile, each CTA runs a contiguous share of the K-groups, and the partial FP32
