@@ -43,14 +43,16 @@
  *     mask out of range, bad K segments) and internal wait time-outs never trap: the
  *     kernel skips the offending tile (or the whole call), records the first such
  *     event in a per-device status word and returns; fg_get_device_error reads it.
- *   - Results are deterministic: no atomics touch D; when a dense GEMM with few tiles
- *     is split along K, the partial tiles are summed in a fixed order.
+ *   - Results are deterministic: every element of D is written once by one tile (with D
+ *     aliasing C, added onto once by one TMA reduce-add); when a dense GEMM with few
+ *     tiles is split along K, the partial tiles are summed in a fixed order.
  *   - Environment switches (tuning and diagnosis aids; the defaults are the measured
  *     best): FG_FORCE_BN=64|128|192|224|256 forces the N tile where that width applies;
  *     FG_FORCE_SPLIT=1|2|4|8 forces the dense split-K cluster size (a split that cannot
- *     run falls back to the cost model); FG_PRINT_CONFIGS=1 prints each launch's tiling to
- *     stderr.  Only a split
- *     changes the FP32 summation order; every choice stays within the stated tolerance.
+ *     run falls back to the cost model); FG_PREFETCH_B=0 turns off the L2 prefetch of a
+ *     single-tile CTA's B before its grid-dependency wait; FG_PRINT_CONFIGS=1 prints each
+ *     launch's tiling to stderr.  Only a split changes the FP32 summation order; every
+ *     choice stays within the stated tolerance.
  */
 #ifndef FG_H
 #define FG_H
