@@ -425,6 +425,44 @@ class Small(DensePair):
     WITH_C = False
 
 
+class Quant:
+    """The quantise/pack kernels on operands of the benchmark GEMMs' sizes: 1x128 row groups
+    of an activation x[8192, 7168], 128x128 blocks of a weight w[7168, 2048], and 1x128
+    groups along K of a K-grouped operand x[16384, 4096].  HBM-bound streams: one FP32 read,
+    one E4M3 write and the packed scale words."""
+    name = "quant"
+    description = ("FP32 -> E4M3 + packed UE8M0 quantisation: 1x128 rows of [8192, 7168], 128x128 "
+                   "blocks of [7168, 2048], 1x128 columns of [16384, 4096]")
+
+    def __init__(self, torch, fg, seed):
+        import workloads
+        self.torch, self.fg = torch, fg
+        rows_x = workloads.device_normal(seed, (8192, 7168))
+        blk_w = workloads.device_normal(seed + 1, (7168, 2048))
+        col_x = workloads.device_normal(seed + 2, (16384, 4096))
+        u8, i32 = torch.uint8, torch.int32
+        self.items = [
+            ("quant_rows", fg.quantize_1x128_rows, rows_x, torch.empty((8192, 7168), dtype=u8, device="cuda"),
+             torch.zeros((cdiv(7168, 512), align4(8192)), dtype=i32, device="cuda")),
+            ("quant_blocks", fg.quantize_128x128_blocks, blk_w, torch.empty((7168, 2048), dtype=u8, device="cuda"),
+             torch.zeros((1, cdiv(2048, 512), align4(cdiv(7168, 128))), dtype=i32, device="cuda")),
+            ("quant_cols", fg.quantize_1x128_cols, col_x, torch.empty((16384, 4096), dtype=u8, device="cuda"),
+             torch.zeros((cdiv(16384, 512), align4(4096)), dtype=i32, device="cuda")),
+        ]
+        self.parts = [{"name": nm, "flops": 0.0, "bound": "hbm",
+                       "bytes": x.numel() * 4 + q.numel() + sf.numel() * 4} for nm, _f, x, q, sf in self.items]
+        torch.cuda.synchronize()
+
+    def launches(self):
+        return [lambda f=f, x=x, q=q, sf=sf: f(x, q, sf) for _nm, f, x, q, sf in self.items]
+
+    def e2e_io(self):
+        ins = [(x, x.cpu().pin_memory()) for _nm, _f, x, _q, _sf in self.items]
+        outs = [(t, self.torch.empty_like(t, device="cpu").pin_memory())
+                for _nm, _f, _x, q, sf in self.items for t in (q, sf)]
+        return ins, outs
+
+
 class _PrefillLayout(Prefill):
     """The prefill GEMM with its operands stored in another layout (same values, same
     bytes and FLOPs): A as [K, M] for a leading T, B as [K, N] for a trailing N."""
@@ -547,12 +585,13 @@ class ContiguousNN(Contiguous):
                                                                  self.m_indices, self.d)]
 
 
-WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, PrefillNN,
+WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, Quant, PrefillNN,
                                  PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
 
 # The benchmark configurations beside the headline pair (recorded in config.kernels of
 # the default run): (configuration number, workload).
-OTHER_CONFIGS = [(0, "small"), (2, "contiguous"), (3, "masked"), (4, "k_grouped")]
+# (configuration number, or the scope row for the quantisers, which no configuration names)
+OTHER_CONFIGS = [(0, "small"), (2, "contiguous"), (3, "masked"), (4, "k_grouped"), ("NEXT-1", "quant")]
 NOMINAL_HBM_GBS = 8000.0        # the stated HBM roof (about 8 TB/s)
 NOMINAL_FP8_TFLOPS = 4500.0     # the stated dense FP8 tensor roof (about 4.5 PFLOP/s)
 MIN_TIMED_SECONDS = 0.5         # repeat the --steps pass until the timed region lasts this long
@@ -778,7 +817,7 @@ def run_gpu(args):
             if args.workload == "dense_pair" else kernel_entry(p, per_kernel[j] * 1e3, peaks)
     if args.workload == "dense_pair" and not args.no_other_configs:
         for cfg_no, name in OTHER_CONFIGS:
-            owl = WORKLOADS[name](torch, fg, args.seed + 101 * cfg_no + 7919 * rank)
+            owl = WORKLOADS[name](torch, fg, args.seed + 101 * (cfg_no if isinstance(cfg_no, int) else 9) + 7919 * rank)
             ol = owl.launches()
             oflush, onote = flush_for(owl)
             for _ in range(args.warmup):

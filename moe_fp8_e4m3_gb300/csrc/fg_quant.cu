@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "fg.h"
 #include "fg_fp8.cuh"
@@ -71,82 +72,116 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float* __restrict
     if (lane == 0) sf[(long long)w * sf_ld + row] = static_cast<int32_t>(byte | b1 << 8 | b2 << 16 | b3 << 24);
 }
 
-// One CTA (8 warps) per (group, 128-row block, packed word): up to four 128x128 blocks.
+// The scale byte of K-group kg goes straight into its packed word (byte kg mod 4); the CTA
+// of the last K-group also clears the word's bytes of K-groups past K, so every word ends
+// up fully defined whatever the buffer held.
+__device__ __forceinline__ void put_scale_byte(uint8_t* word, int kg, int num_kg, int e) {
+    word[kg & 3] = static_cast<uint8_t>(e + 127);
+    if (kg == num_kg - 1)
+        for (int b = (kg & 3) + 1; b < 4; ++b) word[b] = 0;
+}
+
+// One CTA (8 warps, 16 rows each) per 128x128 block: (K-group, 128-row block, group).
 __global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restrict__ w, int N, int K,
                                                            uint8_t* __restrict__ q, int32_t* __restrict__ sf,
-                                                           int sf_ld, int kp, int nblk) {
+                                                           int sf_ld, int kp) {
     __shared__ float red[8];
-    const int g = blockIdx.z, nb = blockIdx.y, wd = blockIdx.x;
+    const int kg = blockIdx.x, nb = blockIdx.y, g = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* base = w + (long long)g * N * K;
     uint8_t* qbase = q + (long long)g * N * K;
-    uint32_t word = 0;
-    for (int j = 0; j < 4; ++j) {
-        const int kg = wd * 4 + j;
-        if (kg * 128 >= K) break;
-        float v[16][4];
-        float amax = 0.0f;
+    float v[16][4];
+    float amax = 0.0f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int row = nb * 128 + warp * 16 + r;
-            if (row < N) {
-                const float4 t = __ldg(reinterpret_cast<const float4*>(base + (long long)row * K + kg * 128) + lane);
-                v[r][0] = t.x; v[r][1] = t.y; v[r][2] = t.z; v[r][3] = t.w;
-            } else {
-                v[r][0] = v[r][1] = v[r][2] = v[r][3] = 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[r][i]));
+    for (int r = 0; r < 16; ++r) {
+        const int row = nb * 128 + warp * 16 + r;
+        if (row < N) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(base + (long long)row * K + kg * 128) + lane);
+            v[r][0] = t.x; v[r][1] = t.y; v[r][2] = t.z; v[r][3] = t.w;
+        } else {
+            v[r][0] = v[r][1] = v[r][2] = v[r][3] = 0.0f;
         }
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) red[warp] = amax;
-        __syncthreads();
-        amax = red[0];
+        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[r][i]));
+    }
 #pragma unroll
-        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-        __syncthreads();
-        const int e = scale_exponent(amax);
-        word |= static_cast<uint32_t>(e + 127) << (8 * j);
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int row = nb * 128 + warp * 16 + r;
-            if (row < N) {
-                uint32_t b = 0;
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const int e = scale_exponent(amax);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) b |= e4m3(ldexpf(v[r][i], -e)) << (8 * i);
-                *reinterpret_cast<uint32_t*>(qbase + (long long)row * K + kg * 128 + lane * 4) = b;
-            }
+    for (int r = 0; r < 16; ++r) {
+        const int row = nb * 128 + warp * 16 + r;
+        if (row < N) {
+            uint32_t b = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) b |= e4m3(ldexpf(v[r][i], -e)) << (8 * i);
+            *reinterpret_cast<uint32_t*>(qbase + (long long)row * K + kg * 128 + lane * 4) = b;
         }
     }
-    if (threadIdx.x == 0) sf[((long long)g * kp + wd) * sf_ld + nb] = static_cast<int32_t>(word);
-    (void)nblk;
+    if (threadIdx.x == 0)
+        put_scale_byte(reinterpret_cast<uint8_t*>(sf + ((long long)g * kp + kg / 4) * sf_ld + nb), kg, K / 128, e);
 }
 
-// One thread per column of x[K][MN]; a CTA covers 256 columns of one packed word (512
-// rows).  Two passes per 128-row group: amax, then encode (the second read hits L2).
+// One CTA per (128-row K-group, 128 columns) of x[K][MN]: the tile is read from HBM once,
+// straight into shared memory by 16-byte cp.async copies (all in flight together), each
+// thread takes one column's amax there, and the codes leave as one 4-code word per row and
+// four columns (coalesced).  64 KB per CTA: three CTAs share an SM, so one's copies overlap
+// another's encoding.
+constexpr int kColTile = 128;                     // columns per CTA
+constexpr int kColSmem = 128 * kColTile * 4 + kColTile * 4;
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_copies() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __global__ void __launch_bounds__(256) quant_cols_kernel(const float* __restrict__ x, int K, int MN,
                                                          uint8_t* __restrict__ q, int32_t* __restrict__ sf,
                                                          int sf_ld) {
-    const int col = blockIdx.x * 256 + threadIdx.x;
-    const int wd = blockIdx.y;
-    if (col >= MN) return;
-    uint32_t word = 0;
-    for (int j = 0; j < 4; ++j) {
-        const int kg = wd * 4 + j;
-        if (kg * 128 >= K) break;
-        const float* src = x + (long long)kg * 128 * MN + col;
+    extern __shared__ __align__(16) float tile[];  // [128][kColTile], then the exponents
+    int* ex = reinterpret_cast<int*>(tile + 128 * kColTile);
+    const int kg = blockIdx.x;
+    const int c0 = blockIdx.y * kColTile;
+    const int ncols = min(kColTile, MN - c0);      // a multiple of 16
+    const int t = threadIdx.x;
+    const float* src = x + (long long)kg * 128 * MN + c0;
+    // stage: 128 rows x ncols/4 float4 groups; thread t copies group t % 32 of rows t / 32 + 8i
+    const int g4 = t & 31, r0 = t >> 5;
+    const uint32_t tile_u32 = static_cast<uint32_t>(__cvta_generic_to_shared(tile));
+    if (4 * g4 < ncols) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = r0 + 8 * i;
+            cp_async_16(tile_u32 + static_cast<uint32_t>((r * kColTile + 4 * g4) * 4), src + (long long)r * MN + 4 * g4);
+        }
+    }
+    cp_async_wait_all_copies();
+    __syncthreads();
+    if (t < ncols) {
         float amax = 0.0f;
 #pragma unroll 8
-        for (int r = 0; r < 128; ++r) amax = fmaxf(amax, fabsf(__ldg(src + (long long)r * MN)));
+        for (int r = 0; r < 128; ++r) amax = fmaxf(amax, fabsf(tile[r * kColTile + t]));
         const int e = scale_exponent(amax);
-        word |= static_cast<uint32_t>(e + 127) << (8 * j);
-        uint8_t* dst = q + (long long)kg * 128 * MN + col;
-#pragma unroll 8
-        for (int r = 0; r < 128; ++r)
-            dst[(long long)r * MN] = static_cast<uint8_t>(e4m3(ldexpf(__ldg(src + (long long)r * MN), -e)));
+        ex[t] = e;
+        put_scale_byte(reinterpret_cast<uint8_t*>(sf + (long long)(kg / 4) * sf_ld + c0 + t), kg, K / 128, e);
     }
-    sf[(long long)wd * sf_ld + col] = static_cast<int32_t>(word);
+    __syncthreads();
+    uint8_t* dst = q + (long long)kg * 128 * MN + c0;
+    if (4 * g4 < ncols) {
+        const int e0 = ex[4 * g4], e1 = ex[4 * g4 + 1], e2 = ex[4 * g4 + 2], e3 = ex[4 * g4 + 3];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = r0 + 8 * i;
+            const float4 v = reinterpret_cast<const float4*>(tile + r * kColTile)[g4];
+            *reinterpret_cast<uint32_t*>(dst + (long long)r * MN + 4 * g4) =
+                e4m3(ldexpf(v.x, -e0)) | e4m3(ldexpf(v.y, -e1)) << 8 | e4m3(ldexpf(v.z, -e2)) << 16 |
+                e4m3(ldexpf(v.w, -e3)) << 24;
+        }
+    }
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -184,8 +219,8 @@ int fg_quantize_128x128_blocks(int G, int N, int K, const float* w, uint8_t* q, 
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return FG_ERR_CUDA; }
     const int kp = (K + 511) / 512, nblk = (N + 127) / 128;
     if (nblk > 65535) return FG_ERR_INVALID_ARG;
-    quant_blocks_kernel<<<dim3(kp, nblk, G), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        w, N, K, q, sf, align4(nblk), kp, nblk);
+    quant_blocks_kernel<<<dim3(K / 128, nblk, G), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w, N, K, q, sf, align4(nblk), kp);
     return finish_launch();
 }
 
@@ -196,9 +231,23 @@ int fg_quantize_1x128_cols(int K, int MN, const float* x, uint8_t* q, int32_t* s
     if (K == 0) return FG_OK;
     int dev;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return FG_ERR_CUDA; }
-    const int kp = (K + 511) / 512;
-    if (kp > 65535) return FG_ERR_INVALID_ARG;
-    quant_cols_kernel<<<dim3((MN + 255) / 256, kp), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    const int cblk = (MN + kColTile - 1) / kColTile;
+    if (cblk > 65535) return FG_ERR_INVALID_ARG;
+    if (dev < 0 || dev >= 256) return FG_ERR_CUDA;
+    {   // the staged tile's shared memory, allowed once per device
+        static std::mutex mu;
+        static bool configured[256] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            if (cudaFuncSetAttribute(quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return FG_ERR_CUDA;
+            }
+            configured[dev] = true;
+        }
+    }
+    quant_cols_kernel<<<dim3(K / 128, cblk), 256, kColSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
         x, K, MN, q, sf, align4(MN));
     return finish_launch();
 }
