@@ -431,9 +431,117 @@ def check_mqa_closed_form():
     assert np.array_equal(neg, np.zeros_like(neg))
 
 
+# ------------------------------------------------------------ FP8 x FP4
+GOLDEN_FP4 = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fp4_closed_forms.json")))
+
+
+def fr_e2m1(code: int) -> Fraction:
+    """E2M1 from its bit fields: sign bit 3, exponent bits 1-2 (bias 1), mantissa bit 0."""
+    code = int(code)
+    s, e, m = code >> 3 & 1, (code >> 1) & 3, code & 1
+    mag = Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1)
+    return -mag if s else mag
+
+
+def fp4_code(b_row: np.ndarray, kk: int) -> int:
+    """Code kk of a packed row: byte kk // 2, low nibble for even kk, high for odd."""
+    return (int(b_row[kk // 2]) >> (4 * (kk % 2))) & 0xF
+
+
+def exact_fp4_dense(a, sfa, b, sfb, c, m, n) -> Fraction:
+    """Element (m, n) of C + A @ B.T with A E4M3 (1x128 scales) and B packed E2M1 with one
+    scale per 32-block of each row (block j is byte j % 4 of word j // 4)."""
+    k = a.shape[1]
+    tot = Fraction(0) if c is None else Fraction(float(c[m, n]))
+    for kk in range(k):
+        tot += (fr_e4m3(a[m, kk]) * fr_ue8(word_byte(sfa, kk // 128, m)) *
+                fr_e2m1(fp4_code(b[n], kk)) * fr_ue8(word_byte(sfb, kk // 32, n)))
+    return tot
+
+
+def rand_fp4(g, shape):
+    return g.integers(0, 256, shape, dtype=np.uint8)
+
+
+def check_fp4_format_golden():
+    from oracle import fp4
+    for row in GOLDEN_FP4["e2m1"]:
+        assert fp4.e2m1_to_f64(np.array([int(row["code"], 16)]))[0] == row["value"], row
+    for row in GOLDEN_FP4["e2m1_rounding"]:
+        assert int(fp4.f64_to_e2m1(np.array([row["x"]]))[0]) == int(row["code"], 16), row
+
+
+def check_fp4_golden_gemm():
+    import oracle
+    from oracle.formats import pack_ue8m0
+    for case in GOLDEN_FP4["gemm_nt"]:
+        m, n, k = case["M"], case["N"], case["K"]
+        a = np.empty((m, k), np.uint8)
+        a[:, 0::2] = int(case["a_even"], 16)
+        a[:, 1::2] = int(case["a_odd"], 16)
+        b = np.full((n, k // 2), int(case["b_byte"], 16), np.uint8)
+        sfa = pack_ue8m0(np.tile(np.array(case["sa"], np.uint8), (m, 1)))
+        sfb = pack_ue8m0(np.tile(np.array(case["sb"], np.uint8), (n, 1)))
+        c = None if case["c"] is None else np.full((m, n), case["c"], np.float32)
+        d = oracle.fp8_fp4_gemm_nt(a, sfa, b, sfb, c)
+        assert np.all(d == case["expect"]), (case["name"], d)
+
+
+def check_fp4_dense_brute_force(seed=10):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    for (m, n, k, with_c) in [(3, 5, 128, False), (2, 9, 256, True), (4, 3, 384, False)]:
+        a, b = rand_codes(g, (m, k)), rand_fp4(g, (n, k // 2))
+        sfa, sfb = rand_words(g, m, k // 128), rand_words(g, n, k // 32)
+        c = g.standard_normal((m, n)).astype(np.float32) if with_c else None
+        d = oracle.fp8_fp4_gemm_nt(a, sfa, b, sfb, c)
+        bits = oracle.round_output(d, "bf16")
+        for i in range(m):
+            for j in range(n):
+                ex = exact_fp4_dense(a, sfa, b, sfb, c, i, j)
+                mag = sum(abs(fr_e4m3(a[i, kk]) * fr_e2m1(fp4_code(b[j], kk))) for kk in range(k)) * Fraction(2) ** 40
+                assert close_fp64(d[i, j], ex, mag, k), (m, n, k, i, j)
+                assert bits[i, j] == fr_to_bf16_bits(ex), (i, j)
+
+
+def check_fp4_grouped_brute_force(seed=11):
+    import oracle
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, n, k = 3, 5, 256
+    m_indices = np.array([2, 2, -1, 0, 0, 0, -1, 1], dtype=np.int32)
+    m_total = len(m_indices)
+    a = rand_codes(g, (m_total, k))
+    b = rand_fp4(g, (num_groups, n, k // 2))
+    sfa = rand_words(g, m_total, k // 128)
+    sfb = np.stack([rand_words(g, n, k // 32) for _ in range(num_groups)])
+    d, written = oracle.m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, m_indices)
+    assert list(written) == [e >= 0 for e in m_indices]
+    for i in range(m_total):
+        e = m_indices[i]
+        if e < 0:
+            assert np.all(np.isnan(d[i]))
+            continue
+        for j in range(n):
+            ex = exact_fp4_dense(a, sfa, b[e], sfb[e], None, i, j)
+            assert abs(Fraction(d[i, j]) - ex) <= abs(ex) * Fraction(1, 2 ** 45) + Fraction(1, 2 ** 900)
+    m_max = 4
+    masked_m = np.array([3, 0, 4])
+    a3 = rand_codes(g, (num_groups, m_max, k))
+    sfa3 = np.stack([rand_words(g, m_max, k // 128) for _ in range(num_groups)])
+    out = oracle.m_grouped_fp8_fp4_gemm_nt_masked(a3, sfa3, b, sfb, masked_m)
+    for e in range(num_groups):
+        assert out[e].shape == (masked_m[e], n)
+        for i in range(masked_m[e]):
+            for j in range(n):
+                ex = exact_fp4_dense(a3[e], sfa3[e], b[e], sfb[e], None, i, j)
+                assert abs(Fraction(out[e][i, j]) - ex) <= abs(ex) * Fraction(1, 2 ** 45) + Fraction(1, 2 ** 900)
+
+
 ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_force,
               check_mqa_brute_force, check_mqa_closed_form,
               check_silu_library, check_swiglu_brute_force, check_swiglu_exact_probe,
               check_contiguous_nn_brute_force, check_contiguous_brute_force,
               check_masked_brute_force, check_k_grouped_brute_force, check_identity,
-              check_one_hot, check_scale_probe, check_integer_valued]
+              check_one_hot, check_scale_probe, check_integer_valued,
+              check_fp4_format_golden, check_fp4_golden_gemm, check_fp4_dense_brute_force,
+              check_fp4_grouped_brute_force]

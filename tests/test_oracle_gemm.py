@@ -182,6 +182,37 @@ def _mqa_scale_dropped(q, kv, kv_sf, weights, ks, ke, clean_logits=True, rows=No
 
 _orig_mqa = MQ.fp8_mqa_logits
 
+import oracle.fp4 as FP4
+
+
+def _fp4_unpack_swapped(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p >> 4
+    out[..., 1::2] = p & 0xF
+    return out
+
+
+def _fp4_scales_per_128(sfb_words, n, k):
+    # one scale per 128-wide K-group (the FP8 activation granularity) instead of per 32
+    s = F.unpack_ue8m0(sfb_words, n, k // 32)
+    return np.repeat(s[:, 0::4], 4, axis=1)
+
+
+def _e2m1_bias_2():
+    return FP4.E2M1_TABLE / 2
+
+
+def _e2m1_subnormal_one():
+    t = FP4.E2M1_TABLE.copy()
+    t[1], t[9] = 1.0, -1.0
+    return t
+
+
+def _fp4_scale_dropped(packed, sf_bytes):
+    return FP4.e2m1_to_f64(FP4.unpack_fp4(packed))
+
+
 MUTANTS = {
     "mqa_relu_dropped": [(MQ, "fp8_mqa_logits", lambda: _mqa_no_relu)],
     "mqa_range_end_inclusive": [(MQ, "fp8_mqa_logits", lambda: _mqa_range_inclusive)],
@@ -203,6 +234,11 @@ MUTANTS = {
     "k_offsets_shifted": [(G, "k_grouped_fp8_gemm_tn_contiguous", lambda: _kg_shifted_offsets)],
     "padding_rows_computed": [(G, "m_grouped_fp8_gemm_nt_contiguous", lambda: _contig_pad_as_expert0)],
     "row_scales_wrong_row": [(G, "row_scales", lambda: _row_scale_transposed)],
+    "fp4_nibbles_swapped": [(FP4, "unpack_fp4", lambda: _fp4_unpack_swapped)],
+    "fp4_scale_per_128": [(FP4, "mx_scales", lambda: _fp4_scales_per_128)],
+    "e2m1_bias_2": [(FP4, "E2M1_TABLE", _e2m1_bias_2)],
+    "e2m1_subnormal_is_one": [(FP4, "E2M1_TABLE", _e2m1_subnormal_one)],
+    "fp4_scale_dropped": [(FP4, "dequant_mxfp4", lambda: _fp4_scale_dropped)],
 }
 
 
