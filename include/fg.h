@@ -233,6 +233,39 @@ int fg_k_grouped_fp8_gemm_tn_contiguous(int G, int M, int N, int K_total,
                                         fg_stream_t stream);
 
 /*
+ * FP8 x FP4 GEMMs: E4M3 activations times FP4 weights.  The pages name an FP8xFP4 GEMM
+ * (Korean README translation, news of 2026.04.16; yuguo-Jack/DeepGEMM README, "News") and
+ * give the Mega MoE's linear layers as FP8 x FP4 with weights in "FP4 with UE8M0 SF"
+ * (Chinese post, "Mega MoE": mma_type 'fp8xfp4'; same README, "CUDA Mega MoE").  Each call
+ * computes what its FP8 counterpart above computes, with B read as:
+ *   - FP4 = E2M1 (OCP Microscaling element: sign, 2 exponent bits with bias 1, 1 mantissa
+ *     bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no inf or NaN), two codes per byte along
+ *     K: element 2i in bits 0-3, 2i+1 in bits 4-7.  b is [N][K/2] bytes ([G][N][K/2]).
+ *   - one UE8M0 scale per 32 consecutive K elements of each row of B (the MXFP4 block),
+ *     packed four per int32 (byte j of word w = block 4w+j, i.e. one word per row and
+ *     128-wide K-group), MN-major: sfb [K/128][align4(N)] int32 ([G][K/128][align4(N)]).
+ * a, sfa, c, d, m_indices, masked_m, expected_m, the shape rules, the device contract and
+ * the status reporting are those of fg_fp8_gemm_nt, fg_m_grouped_fp8_gemm_nt_contiguous and
+ * fg_m_grouped_fp8_gemm_nt_masked.  b must be 32-byte aligned (FG_ERR_INVALID_ARG
+ * otherwise).  The accumulation is FP32 in the tensor core with both scales applied per
+ * 32-wide K step.
+ */
+int fg_fp8_fp4_gemm_nt(int M, int N, int K,
+                       const uint8_t* a, const int32_t* sfa,
+                       const uint8_t* b, const int32_t* sfb,
+                       const float* c, void* d, int d_dtype, fg_stream_t stream);
+int fg_m_grouped_fp8_fp4_gemm_nt_contiguous(int M_total, int N, int K, int G,
+                                            const uint8_t* a, const int32_t* sfa,
+                                            const uint8_t* b, const int32_t* sfb,
+                                            const int32_t* m_indices,
+                                            void* d, int d_dtype, fg_stream_t stream);
+int fg_m_grouped_fp8_fp4_gemm_nt_masked(int G, int M_max, int N, int K,
+                                        const uint8_t* a, const int32_t* sfa,
+                                        const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* masked_m, int expected_m,
+                                        void* d, int d_dtype, fg_stream_t stream);
+
+/*
  * FP32 -> E4M3 quantisation with UE8M0 scales, written straight into the packed,
  * MN-major, TMA-aligned scale layout the GEMMs above read.  The pages leave the FP8
  * cast to the user and list layout helpers for it ("DeepGEMM Documentation", section

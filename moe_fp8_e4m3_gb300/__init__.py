@@ -36,6 +36,9 @@ _SIGNATURES = {
     "fg_fp8_mqa_logits": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked_swiglu": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_m_grouped_fp8_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
+    "fg_fp8_fp4_gemm_nt": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_m_grouped_fp8_fp4_gemm_nt_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "fg_m_grouped_fp8_fp4_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
     "fg_k_grouped_fp8_gemm_tn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_quantize_1x128_rows": (_I, [_I, _I, _P, _P, _P, _P]),
     "fg_quantize_128x128_blocks": (_I, [_I, _I, _I, _P, _P, _P, _P]),
@@ -222,6 +225,49 @@ def m_grouped_fp8_gemm_nt_masked(a, sfa, b, sfb, masked_m, d, expected_m=0, stre
     _check(lib.fg_m_grouped_fp8_gemm_nt_masked(g, m_max, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb),
                                                _ptr(masked_m), int(expected_m), _ptr(d), code,
                                                _stream(stream)), "m_grouped_fp8_gemm_nt_masked")
+
+
+def _fp4(t, name):
+    import torch
+    ok = t.dtype == torch.uint8 or t.dtype == getattr(torch, "float4_e2m1fn_x2", torch.uint8)
+    if not ok or not t.is_contiguous() or not t.is_cuda:
+        raise TypeError(f"{name} must be a contiguous CUDA uint8/float4_e2m1fn_x2 tensor of packed E2M1 pairs")
+
+
+def fp8_fp4_gemm_nt(a, sfa, b, sfb, d, c=None, stream=None) -> None:
+    """D = C + A @ B.T with FP4 B.  a [M,K] E4M3, sfa as fp8_gemm_nt; b [N,K/2] packed E2M1
+    (element 2i in the low nibble); sfb [K/128, align4(N)] int32, one UE8M0 scale per 32 K
+    elements of each row of B; d [M,N] BF16/FP32; c optional FP32 [M,N] (FP32 d only)."""
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _c(c)
+    code = _out(d, "d")
+    m, k = a.shape
+    n = b.shape[0]
+    _check(lib.fg_fp8_fp4_gemm_nt(m, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                  code, _stream(stream)), "fp8_fp4_gemm_nt")
+
+
+def m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, m_indices, d, stream=None) -> None:
+    """The M-grouped contiguous GEMM with FP4 B.  a [M_total,K]; b [G,N,K/2] packed E2M1;
+    sfb [G, K/128, align4(N)] int32 (1x32 blocks); m_indices int32 [M_total]."""
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _i32(m_indices, "m_indices")
+    code = _out(d, "d")
+    m_total, k = a.shape
+    g, n, _ = b.shape
+    _check(lib.fg_m_grouped_fp8_fp4_gemm_nt_contiguous(m_total, n, k, g, _ptr(a), _ptr(sfa), _ptr(b),
+                                                       _ptr(sfb), _ptr(m_indices), _ptr(d), code,
+                                                       _stream(stream)), "m_grouped_fp8_fp4_gemm_nt_contiguous")
+
+
+def m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, masked_m, d, expected_m=0, stream=None) -> None:
+    """The M-grouped masked GEMM with FP4 B.  a [G,M_max,K]; b [G,N,K/2] packed E2M1;
+    sfb [G, K/128, align4(N)] int32 (1x32 blocks); masked_m int32 [G] on the device."""
+    _fp8(a, "a"); _fp4(b, "b"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _i32(masked_m, "masked_m")
+    code = _out(d, "d")
+    g, m_max, k = a.shape
+    n = b.shape[1]
+    _check(lib.fg_m_grouped_fp8_fp4_gemm_nt_masked(g, m_max, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb),
+                                                   _ptr(masked_m), int(expected_m), _ptr(d), code,
+                                                   _stream(stream)), "m_grouped_fp8_fp4_gemm_nt_masked")
 
 
 def k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, ks, d, c=None, stream=None) -> None:

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfg.so")
 SOURCES = ["fg_api.cu", "fg_gemm_nt.cu", "fg_gemm_split.cu", "fg_gemm_tn.cu", "fg_gemm_layouts.cu",
-           "fg_gemm_sepc.cu", "fg_gemm_dense.cu", "fg_gemm_swiglu.cu", "fg_mqa.cu", "fg_quant.cu"]
+           "fg_gemm_sepc.cu", "fg_gemm_dense.cu", "fg_gemm_swiglu.cu", "fg_gemm_fp4.cu", "fg_gemm_fp4_grouped.cu",
+           "fg_mqa.cu", "fg_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -207,13 +207,17 @@ int forced_split() {
 // output) it is not considered.  Measured on GB300: 4096 x 7168 x 2048 FP32 D without C,
 // BN=224 67 us against BN=256 74 us; BF16 D, masked 32 x 256 x 4096 x 2048 62.1 us against
 // 63.9 us and contiguous 32 x 4096 x 4096 137.9 us against 140.2 us.
-int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue) {
+// The FP8 x FP4 variants exist at two widths, 128 and 224 (fp4 restricts the choice to them).
+bool fp4_width(int bn) { return bn == 128 || bn == 224; }
+
+int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue, bool fp4 = false) {
     const int f = forced_bn();
-    if (f == 64 || f == 128 || f == 192 || f == 224 || f == 256) return f;
+    if ((f == 64 || f == 128 || f == 192 || f == 224 || f == 256) && (!fp4 || fp4_width(f))) return f;
     int best = 128;
     double best_cost = -1.0;
     for (int bn : {224, 256, 192, 128, 64}) {
         if (heavy_epilogue && bn == 256) continue;
+        if (fp4 && !fp4_width(bn)) continue;
         const long long tiles = row_blocks * ceil_div(n, bn);
         const long long waves = (tiles + sms - 1) / sms;
         const double cost = static_cast<double>(waves * (bn + 32)) * (bn == 256 ? 1.15 : 1.0);
@@ -246,15 +250,18 @@ struct DenseTiling {
     int bn;
     int split;
 };
-DenseTiling choose_dense_tiling(DeviceState& st, int num_mb, int n, int k, int sms, bool heavy_epilogue) {
+// fp4: the FP8 x FP4 variants (unsplit at 128 and 224, split-K clusters at 128).
+DenseTiling choose_dense_tiling(DeviceState& st, int num_mb, int n, int k, int sms, bool heavy_epilogue,
+                                bool fp4 = false) {
     const int fb = forced_bn(), fs = forced_split();
     const int nkb = k / 128;
-    DenseTiling best{choose_bn_nt(num_mb, n, sms, heavy_epilogue), 1};
+    DenseTiling best{choose_bn_nt(num_mb, n, sms, heavy_epilogue, fp4), 1};
     const long long tiles1 = (long long)num_mb * ceil_div(n, best.bn);
     double best_t = (double)((tiles1 + sms - 1) / sms) * nkb * t_kb_us(best.bn);
     if (fs == 1) return best;
     for (int bn : {256, 224, 192, 128, 64}) {
         if (fb && bn != fb) continue;
+        if (fp4 && bn != 128) continue;
         const long long tiles = (long long)num_mb * ceil_div(n, bn);
         for (int s : {2, 4, 8}) {
             if (fs && s != fs) continue;
@@ -308,6 +315,30 @@ cudaError_t launch_nt_bn(int bn, const GemmParams& p, const fg::GemmMaps& gm, in
         case 224: return fg::launch_gemm<224, fg::kMajNT, kSplit, false, kSepC, kKind>(p, gm, grid, s);
         default: return fg::launch_gemm<256, fg::kMajNT, kSplit, false, false, kKind>(p, gm, grid, s);
     }
+}
+
+// One FP8 x FP4 launch (B packed E2M1): tile width 128 or 224, split-K clusters at 128.
+template <bool kSplit, bool kSepC, int kKind>
+cudaError_t launch_fp4_bn(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    if (bn == 128) return fg::launch_gemm<128, fg::kMajNTF4, kSplit, false, kSepC, kKind>(p, gm, grid, s);
+    if constexpr (!kSplit) {
+        if (bn == 224) return fg::launch_gemm<224, fg::kMajNTF4, false, false, kSepC, kKind>(p, gm, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+int launch_fp4(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    cudaError_t e;
+    if (p.split > 1) e = launch_fp4_bn<true, false, fg::kDense>(bn, p, gm, grid, s);
+    else if (p.kind == fg::kContiguous) e = launch_fp4_bn<false, false, fg::kContiguous>(bn, p, gm, grid, s);
+    else if (p.kind == fg::kMasked) e = launch_fp4_bn<false, false, fg::kMasked>(bn, p, gm, grid, s);
+    else if (separate_c(p)) e = launch_fp4_bn<false, true, fg::kDense>(bn, p, gm, grid, s);
+    else e = launch_fp4_bn<false, false, fg::kDense>(bn, p, gm, grid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FG_ERR_CUDA;
+    }
+    return FG_OK;
 }
 
 int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
@@ -386,25 +417,42 @@ int launch_mn(int maj, int bn, const GemmParams& p, const fg::GemmMaps& gm, int 
     return FG_OK;
 }
 
-// Shared checks of the NT operands: FP8 A/B and the packed scale arrays.
+// Shared checks of the NT operands: FP8 A/B and the packed scale arrays.  Packed FP4 B
+// (fp4) must start on a 32-byte boundary (the unpacking TMA form's rule).
 int check_nt_operands(int n, int k, const void* a, const void* sfa, const void* b,
-                      const void* sfb, const void* d, int d_dtype) {
+                      const void* sfb, const void* d, int d_dtype, bool fp4 = false) {
     if (n < 16 || n % 16 != 0 || k < 128 || k % 128 != 0) return FG_ERR_INVALID_ARG;
     if (d_dtype != FG_BF16 && d_dtype != FG_F32) return FG_ERR_INVALID_ARG;
     if (!a || !sfa || !b || !sfb || !d) return FG_ERR_INVALID_ARG;
     if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d))
         return FG_ERR_INVALID_ARG;
+    if (fp4 && (reinterpret_cast<uintptr_t>(b) & 31u) != 0) return FG_ERR_INVALID_ARG;
     return FG_OK;
 }
 
-}  // namespace
+// B tensor map of an NT call over `rows` rows of K: E4M3 bytes, or packed E2M1 codes (fp4)
+// unpacked by the TMA unit into 16-byte chunks of 16 codes (8 bytes of codes, 8 of padding),
+// the shared-memory form of a sub-byte tcgen05 operand, so a 128-code box row takes 128 bytes.
+bool encode_b_nt(CUtensorMap* map, const void* b, int K, uint64_t rows, int bn, bool fp4) {
+    if (fp4)
+        return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, b, K, rows, (uint64_t)K / 2, 128, bn,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, rows, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
-extern "C" {
+// B scales: one per 128x128 block, packed per four K-groups; FP4 B: one per row and 32-wide
+// block, one word (four blocks) per row and K-group.
+void set_b_scales(GemmParams& p, int N, int K, bool fp4) {
+    p.sfb_ld = fp4 ? align4(N) : align4(ceil_div(N, 128));
+    p.sfb_per_row = fp4 ? 1 : 0;
+    p.sfb_gstride = (long long)(fp4 ? K / 128 : ceil_div(K, 512)) * p.sfb_ld;
+}
 
-int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
-                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+// Dense NT GEMM; fp4: B packed E2M1 with 1x32 scales (the FP8 x FP4 GEMM).
+int dense_nt(bool fp4, int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+             const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
     if (M < 0) return FG_ERR_INVALID_ARG;
-    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype, fp4);
     if (rc) return rc;
     if (c && !aligned16(c)) return FG_ERR_INVALID_ARG;
     if (c && d_dtype != FG_F32) return FG_ERR_UNSUPPORTED;
@@ -413,7 +461,7 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int num_mb = ceil_div(M, 128);
-    const DenseTiling tiling = choose_dense_tiling(*st, num_mb, N, K, sms, c != nullptr || d_dtype == FG_F32);
+    const DenseTiling tiling = choose_dense_tiling(*st, num_mb, N, K, sms, c != nullptr || d_dtype == FG_F32, fp4);
     const int bn = tiling.bn;
     GemmParams p{};
     fill_common(p, *st);
@@ -424,7 +472,8 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     p.num_mb = num_mb;
     p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
-    p.sfa_ld = align4(M); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_ld = align4(M);
+    set_b_scales(p, N, K, fp4);
     p.sfa_rows = M;
     p.d = d;
     p.c = c;
@@ -437,7 +486,7 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M, K, 128, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_b_nt(&mb, b, K, N, bn, fp4) ||
         !encode_d_maps(gm, d, N, M, p.d_f32) || (c && !encode_c_maps(gm, c, N, M)))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
@@ -446,21 +495,19 @@ int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     // one tile per CTA (or cluster): its B can be prefetched into L2 before the dependency wait
     p.prefetch_b = g_pdl && (p.split > 1 || tiles <= sms) && prefetch_b_enabled();
     if (print_configs())
-        std::fprintf(stderr, "[fg] fp8_gemm_nt M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d\n", M, N, K, bn,
-                     p.split, tiles, grid);
+        std::fprintf(stderr, "[fg] %s M=%d N=%d K=%d BN=%d split=%d tiles=%lld grid=%d\n",
+                     fp4 ? "fp8_fp4_gemm_nt" : "fp8_gemm_nt", M, N, K, bn, p.split, tiles, grid);
+    if (fp4) return launch_fp4(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
-}  // extern "C"
-
-namespace {
-
-// M-grouped contiguous GEMM; b_nmajor: B stored [G][K][N] (NN) instead of [G][N][K] (NT).
-int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const uint8_t* a, const int32_t* sfa,
-                         const uint8_t* b, const int32_t* sfb, const int32_t* m_indices, void* d, int d_dtype,
-                         fg_stream_t stream) {
+// M-grouped contiguous GEMM; b_nmajor: B stored [G][K][N] (NN) instead of [G][N][K] (NT);
+// fp4: B [G][N][K/2] packed E2M1 with 1x32 scales (NT only).
+int m_grouped_contiguous(bool b_nmajor, bool fp4, int M_total, int N, int K, int G, const uint8_t* a,
+                         const int32_t* sfa, const uint8_t* b, const int32_t* sfb, const int32_t* m_indices,
+                         void* d, int d_dtype, fg_stream_t stream) {
     if (M_total < 0 || M_total % 128 != 0 || G < 1) return FG_ERR_INVALID_ARG;
-    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype, fp4);
     if (rc) return rc;
     if (!m_indices || !aligned4(m_indices)) return FG_ERR_INVALID_ARG;
     if ((long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
@@ -470,15 +517,15 @@ int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const 
     const int sms = sms_in_use(*st);
     const int num_mb = M_total / 128;
     const bool heavy = d_dtype == FG_F32;
-    const int bn = b_nmajor ? choose_bn_tn(num_mb, N, sms, heavy) : choose_bn_nt(num_mb, N, sms, heavy);
+    const int bn = b_nmajor ? choose_bn_tn(num_mb, N, sms, heavy) : choose_bn_nt(num_mb, N, sms, heavy, fp4);
     GemmParams p{};
     p.kind = fg::kContiguous;
     p.M = M_total; p.N = N; p.K = K; p.G = G;
     p.d_f32 = d_dtype == FG_F32; p.has_c = 0;
     p.num_mb = num_mb; p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
-    p.sfa_ld = align4(M_total); p.sfb_ld = align4(ceil_div(N, 128));
-    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    p.sfa_ld = align4(M_total);
+    set_b_scales(p, N, K, fp4);
     p.sfa_rows = M_total;
     p.m_indices = m_indices;
     p.d = d;
@@ -489,7 +536,7 @@ int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const 
     CUtensorMap &ma = gm.a, &mb = gm.b;
     const bool b_ok = b_nmajor
         ? encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, N, (uint64_t)G * K, N, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
-        : encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+        : encode_b_nt(&mb, b, K, (uint64_t)G * N, bn, fp4);
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !b_ok || !encode_d_maps(gm, d, N, M_total, p.d_f32))
         return FG_ERR_INVALID_ARG;
@@ -497,8 +544,9 @@ int m_grouped_contiguous(bool b_nmajor, int M_total, int N, int K, int G, const 
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
         std::fprintf(stderr, "[fg] m_grouped_%s_contiguous M_total=%d N=%d K=%d G=%d BN=%d grid=%d\n",
-                     b_nmajor ? "nn" : "nt", M_total, N, K, G, bn, grid);
+                     b_nmajor ? "nn" : (fp4 ? "fp8_fp4_nt" : "nt"), M_total, N, K, G, bn, grid);
     if (b_nmajor) return launch_mn(fg::kMajNN, bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (fp4) return launch_fp4(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -566,14 +614,14 @@ int fg_m_grouped_fp8_gemm_nt_contiguous(int M_total, int N, int K, int G, const 
                                         const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
                                         const int32_t* m_indices, void* d, int d_dtype,
                                         fg_stream_t stream) {
-    return m_grouped_contiguous(false, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
+    return m_grouped_contiguous(false, false, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
 }
 
 int fg_m_grouped_fp8_gemm_nn_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
                                         const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
                                         const int32_t* m_indices, void* d, int d_dtype,
                                         fg_stream_t stream) {
-    return m_grouped_contiguous(true, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
+    return m_grouped_contiguous(true, false, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
 }
 
 int fg_fp8_gemm_nn(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
@@ -591,29 +639,33 @@ int fg_fp8_gemm_tt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, co
     return dense_mn(fg::kMajTT, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
 }
 
-int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
-                                    const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
-                                    const int32_t* masked_m, int expected_m, void* d, int d_dtype,
-                                    fg_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// M-grouped masked GEMM; fp4: B [G][N][K/2] packed E2M1 with 1x32 scales.
+int m_grouped_masked(bool fp4, int G, int M_max, int N, int K, const uint8_t* a, const int32_t* sfa,
+                     const uint8_t* b, const int32_t* sfb, const int32_t* masked_m, int expected_m, void* d,
+                     int d_dtype, fg_stream_t stream) {
     if (G < 1 || G > fg::kMaxGroups || M_max < 1) return FG_ERR_INVALID_ARG;
     if ((long long)G * M_max > 0x7fffffffLL || (long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
-    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype);
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, d, d_dtype, fp4);
     if (rc) return rc;
     if (!masked_m || !aligned4(masked_m)) return FG_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
     if ((rc = device_state(&st))) return rc;
     const int sms = sms_in_use(*st);
     const int hint = expected_m > 0 ? (expected_m < M_max ? expected_m : M_max) : M_max;
-    const int bn = choose_bn_nt((long long)G * ceil_div(hint, 128), N, sms, d_dtype == FG_F32);
+    const int bn = choose_bn_nt((long long)G * ceil_div(hint, 128), N, sms, d_dtype == FG_F32, fp4);
     GemmParams p{};
     p.kind = fg::kMasked;
     p.M = M_max; p.N = N; p.K = K; p.G = G;
     p.d_f32 = d_dtype == FG_F32; p.has_c = 0;
     p.num_mb = ceil_div(M_max, 128); p.num_nb = ceil_div(N, bn);
     p.sfa = sfa; p.sfb = sfb;
-    p.sfa_ld = align4(M_max); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_ld = align4(M_max);
     p.sfa_gstride = (long long)ceil_div(K, 512) * p.sfa_ld;
-    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    set_b_scales(p, N, K, fp4);
     p.sfa_rows = M_max;
     p.masked_m = masked_m;
     p.d = d;
@@ -623,14 +675,51 @@ int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_
     CUtensorMap &ma = gm.a, &mb = gm.b, &mc = gm.c;
     std::memset(&mc, 0, sizeof(mc));
     if (!encode_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b, K, (uint64_t)G * N, K, 128, bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_b_nt(&mb, b, K, (uint64_t)G * N, bn, fp4) ||
         !encode_d_maps(gm, d, N, (long long)G * M_max, p.d_f32))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)G * p.num_mb * p.num_nb;   // upper bound
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
-        std::fprintf(stderr, "[fg] m_grouped_masked G=%d M_max=%d N=%d K=%d BN=%d grid=%d\n", G, M_max, N, K, bn, grid);
+        std::fprintf(stderr, "[fg] m_grouped_%smasked G=%d M_max=%d N=%d K=%d BN=%d grid=%d\n",
+                     fp4 ? "fp8_fp4_" : "", G, M_max, N, K, bn, grid);
+    if (fp4) return launch_fp4(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
     return launch_nt(bn, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fg_fp8_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                   const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    return dense_nt(false, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
+}
+
+int fg_fp8_fp4_gemm_nt(int M, int N, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                       const int32_t* sfb, const float* c, void* d, int d_dtype, fg_stream_t stream) {
+    return dense_nt(true, M, N, K, a, sfa, b, sfb, c, d, d_dtype, stream);
+}
+
+int fg_m_grouped_fp8_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
+                                    const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                    const int32_t* masked_m, int expected_m, void* d, int d_dtype,
+                                    fg_stream_t stream) {
+    return m_grouped_masked(false, G, M_max, N, K, a, sfa, b, sfb, masked_m, expected_m, d, d_dtype, stream);
+}
+
+int fg_m_grouped_fp8_fp4_gemm_nt_masked(int G, int M_max, int N, int K, const uint8_t* a,
+                                        const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                        const int32_t* masked_m, int expected_m, void* d, int d_dtype,
+                                        fg_stream_t stream) {
+    return m_grouped_masked(true, G, M_max, N, K, a, sfa, b, sfb, masked_m, expected_m, d, d_dtype, stream);
+}
+
+int fg_m_grouped_fp8_fp4_gemm_nt_contiguous(int M_total, int N, int K, int G, const uint8_t* a,
+                                            const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                            const int32_t* m_indices, void* d, int d_dtype,
+                                            fg_stream_t stream) {
+    return m_grouped_contiguous(false, true, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
 }
 
 int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G, const uint8_t* a,

@@ -73,8 +73,10 @@ enum GemmKind : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 
 // Operand majors of a kernel variant (the pages' layout letters, D = C + A @ B):
 // bit 0 set = A stored [K][M] (M-major, "T"), clear = [M][K] (K-major, "N");
-// bit 1 set = B stored [K][N] (N-major, "N"), clear = [N][K] (K-major, "T").
-enum : int { kMajNT = 0, kMajTT = 1, kMajNN = 2, kMajTN = 3 };
+// bit 1 set = B stored [K][N] (N-major, "N"), clear = [N][K] (K-major, "T");
+// bit 2 set = B holds FP4 (E2M1) codes, two per byte along K, with one UE8M0 scale per
+// 32 K elements of each row (the FP8 x FP4 GEMM; K-major B only).
+enum : int { kMajNT = 0, kMajTT = 1, kMajNN = 2, kMajTN = 3, kMajNTF4 = 4 };
 
 // Device status codes (the word keeps the first event).
 enum : int {
@@ -516,7 +518,13 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     const CUtensorMap& tm_c = maps.c;
     const CUtensorMap& tm_d = maps.d;
     constexpr bool kAmn = (kMaj & 1) != 0, kBmn = (kMaj & 2) != 0;
-    static_assert(!(kSplit && kMaj != kMajNT), "split-K clusters are a dense NT variant");
+    // FP4 B: the tensor map unpacks every 16 codes (8 bytes) into a 16-byte shared-memory
+    // chunk (the second 8 bytes are padding), so a 128-code K-group row takes the 128 bytes
+    // an E4M3 row takes and the MMA walks the stage exactly as for FP8 B; the instruction
+    // descriptor names E2M1 for B, and each K=32 MMA selects its own scale byte.
+    constexpr bool kFp4B = (kMaj & 4) != 0;
+    static_assert(!kFp4B || (kMaj == kMajNTF4 && !kSwiGLU), "FP4 B is a K-major NT operand");
+    static_assert(!(kSplit && (kMaj & 3) != kMajNT), "split-K clusters are a dense NT variant");
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
     static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
@@ -711,7 +719,12 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdesc = make_idesc_mxf8(128, BN, kAmn, kBmn);
+            constexpr uint32_t kIdesc = make_idesc_mxf8(128, BN, kAmn, kBmn, kFp4B ? kFmtE2M1 : kFmtE4M3);
+            // TMEM scale slots in rotation: FP4 B copies a scale word row at every K-group,
+            // so it rotates over four slots (a slot is rewritten four K-groups after the MMAs
+            // that read it were issued); FP8 scales change every fourth K-group, two slots.
+            constexpr uint32_t kSfSlots = kFp4B ? 4u : 2u;
+            static_assert(C::kSfCol0 + 16 * (kSfSlots - 1) + C::kSfCols <= 512, "TMEM columns of the scale slots");
             // Shared-memory descriptors of stage 0; a stage's descriptor adds its offset in
             // 16-byte units to the start-address field (shared addresses stay below 2^18, so
             // the 14-bit field never carries).  K step j of a stage: K-major operands advance
@@ -734,13 +747,13 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
             // its four MMAs, and the commit that frees it
             auto issue_stage = [&](int kb, uint32_t d_t) {
                 const uint32_t sf_id = static_cast<uint32_t>(tl.kb0 + kb) & 3u;
-                if (kb == 0 || sf_id == 0) {
+                if (kFp4B || kb == 0 || sf_id == 0) {
                     // A packed word holds the scales of four consecutive K-groups: copy it at the
                     // tile's first K-group and at every fourth global K-group, alternating between
                     // two TMEM slots (the copy of the next word never overwrites one still read by
                     // MMAs in flight: tcgen05 operations of one thread execute in issue order).
                     ++kcount;
-                    const uint32_t sfa_n = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                    const uint32_t sfa_n = tmem_base + C::kSfCol0 + (kcount % kSfSlots) * 16;
                     const uint32_t ssfa = sbase + C::kOffSf + s * C::kSfSlotBytes;
                     fence_proxy_async_smem();    // scale words written by cp.async, read by tcgen05.cp
                     tc_cp_32x128b_warpx4(sfa_n, make_sdesc(ssfa, 0, 128, kLayoutNone));
@@ -748,14 +761,17 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     for (int i = 0; i < C::kSfbAtoms; ++i)
                         tc_cp_32x128b_warpx4(sfa_n + 4 + 4 * i, make_sdesc(ssfa + C::kSfaBytes + 512 * i, 0, 128, kLayoutNone));
                 }
-                const uint32_t sfa_t = tmem_base + C::kSfCol0 + (kcount & 1u) * 16;
+                const uint32_t sfa_t = tmem_base + C::kSfCol0 + (kcount % kSfSlots) * 16;
                 const uint32_t sfb_t = sfa_t + 4;
-                const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, sf_id);
                 const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * C::kABytes) >> 4);
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * C::kBBytes) >> 4);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < 4; ++j) {
+                    // A: byte (K-group mod 4) of its word; FP4 B: byte j (the j-th 32-wide block
+                    // of this K-group), otherwise the A choice
+                    const uint32_t idesc = idesc_sf_ids(kIdesc, sf_id, kFp4B ? static_cast<uint32_t>(j) : sf_id);
                     tc_mma_mxf8(d_t, ad + kAStep * j, bd + kBStep * j, idesc, sfa_t, sfb_t, (kb | j) != 0);
+                }
                 tc_commit(empty_bar(s));
                 if (++s == C::kStages) { s = 0; ph ^= 1u; }
             };
@@ -814,7 +830,9 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                     const int kc = (tl.kb0 + kb) * 128;
                     {
                         const uint32_t fb = full_bar(s);
-                        mbar_arrive_expect_tx(fb, C::kBBytes);
+                        // packed FP4 B: the transaction counts the bytes read (two codes per
+                        // byte), half the unpacked bytes the box fills in shared memory
+                        mbar_arrive_expect_tx(fb, kFp4B ? C::kBBytes / 2 : C::kBBytes);
                         if constexpr (kSwiGLU) {
                             // B as [2G halves][I rows][K]: one box of the tile's 128 gate rows
                             // and the matching 128 up rows (half 2g, then 2g + 1)
@@ -860,7 +878,7 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                 // warp-uniform decision: every lane leaves together on abort
                 const bool ok = wait_bar(empty_bar(s), ph ^ 1u, wctl, kWaitScales);
                 if (!__all_sync(0xffffffffu, ok)) { aborted = true; break; }
-                if (kb == 0 || ((tl.kb0 + kb) & 3) == 0) {
+                if (kFp4B || kb == 0 || ((tl.kb0 + kb) & 3) == 0) {
                     const int kw = (tl.kb0 + kb) >> 2;
                     const int32_t* pa = pa0 + (long long)kw * p.sfa_ld;
                     const uint32_t da = sbase + C::kOffSf + s * C::kSfSlotBytes + lane * 16;
@@ -870,7 +888,8 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
                         const bool in = row < p.sfa_rows;
                         cp_async_4(da + 4 * j, in ? pa + row : pa, in ? 4u : 0u);
                     }
-                    const int32_t* pb = pb0 + (long long)kw * p.sfb_ld;
+                    // FP4 B: one word row per K-group (four 32-wide blocks); else per four
+                    const int32_t* pb = pb0 + (long long)(kFp4B ? tl.kb0 + kb : kw) * p.sfb_ld;
                     const uint32_t db = da + C::kSfaBytes;
 #pragma unroll
                     for (int i = 0; i < C::kSfbAtoms; ++i) {

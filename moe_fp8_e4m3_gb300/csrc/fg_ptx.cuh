@@ -297,13 +297,14 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
-// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 x E4M3 (format
-// code 0 at bits 7-9 and 10-12), operand majors at bits 15/16 (0 = K-major,
-// 1 = MN-major), N >> 3 at bits 17-22, UE8M0 scale type (bit 23 = 1), M >> 4 at bits
-// 24-28.  The scale-factor byte selectors go to bits 4-5 (B) and 29-30 (A).
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A is E4M3 (format code 0
+// at bits 7-9), B E4M3 or E2M1 (format code 0 or 5 at bits 10-12), operand majors at bits
+// 15/16 (0 = K-major, 1 = MN-major), N >> 3 at bits 17-22, UE8M0 scale type (bit 23 = 1),
+// M >> 4 at bits 24-28.  The scale-factor byte selectors go to bits 4-5 (B) and 29-30 (A).
+enum : uint32_t { kFmtE4M3 = 0, kFmtE2M1 = 5 };
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(int m, int n, bool a_mn_major,
-                                                       bool b_mn_major) {
-    return (a_mn_major ? 1u : 0u) << 15 | (b_mn_major ? 1u : 0u) << 16 |
+                                                       bool b_mn_major, uint32_t b_fmt = kFmtE4M3) {
+    return (b_fmt & 7u) << 10 | (a_mn_major ? 1u : 0u) << 15 | (b_mn_major ? 1u : 0u) << 16 |
            static_cast<uint32_t>(n >> 3) << 17 | 1u << 23 | static_cast<uint32_t>(m >> 4) << 24;
 }
 // Instruction descriptor of kind::f8f6f4 without block scaling: FP32 accumulator (D

@@ -11,6 +11,7 @@ import numpy as np
 import oracle
 import workloads
 from oracle import formats as F
+from oracle import fp4 as FP4
 
 REL_TOL = 1e-2
 DIFF_TOL = 1e-5
@@ -118,6 +119,55 @@ def k_grouped_case(seed, with_c=True, **kw):
 def k_grouped_ref(case, experts=None, rows=None):
     return oracle.k_grouped_fp8_gemm_tn_contiguous(case["a"], case["sfa"], case["b"], case["sfb"],
                                                    case["ks"], case["c"], experts=experts, rows=rows)
+
+
+# -------------------------------------------------------------- FP8 x FP4
+def _mxfp4_experts(b):
+    """Weights [G, N, K] -> packed E2M1 [G, N, K/2] and packed 1x32 scale words per expert."""
+    packed, words = [], []
+    for e in range(b.shape[0]):
+        q, sf = FP4.quantize_mxfp4(b[e])
+        packed.append(q)
+        words.append(FP4.pack_mx_scales(sf))
+    return np.stack(packed), np.stack(words)
+
+
+def fp4_dense_case(seed, m, n, k, with_c, out="bf16"):
+    w = workloads.dense(seed, m, n, k, with_c)
+    a, sa = F.quantize_rows(w["a"])
+    b, sb = FP4.quantize_mxfp4(w["b"])
+    return {"m": m, "n": n, "k": k, "a": a, "sfa": F.pack_ue8m0(sa), "b": b, "sfb": FP4.pack_mx_scales(sb),
+            "c": w["c"], "out": out}
+
+
+def fp4_dense_ref(case, rows=None):
+    return oracle.fp8_fp4_gemm_nt(case["a"], case["sfa"], case["b"], case["sfb"], case["c"], rows=rows)
+
+
+def fp4_contiguous_case(seed, **kw):
+    """The contiguous routing and activations of :func:`contiguous_case` with MXFP4 weights."""
+    w = workloads.contiguous(seed, **kw)
+    case = contiguous_case(seed, **kw)
+    case["b"], case["sfb"] = _mxfp4_experts(w["b"])
+    return case
+
+
+def fp4_contiguous_ref(case, rows=None):
+    return oracle.m_grouped_fp8_fp4_gemm_nt_contiguous(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                       case["m_indices"], rows=rows)
+
+
+def fp4_masked_case(seed, **kw):
+    """The masked activations of :func:`masked_case` with MXFP4 weights."""
+    w = workloads.masked(seed, **kw)
+    case = masked_case(seed, **kw)
+    case["b"], case["sfb"] = _mxfp4_experts(w["b"])
+    return case
+
+
+def fp4_masked_ref(case, experts=None, rows=None):
+    return oracle.m_grouped_fp8_fp4_gemm_nt_masked(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                   case["masked_m"], experts=experts, rows=rows)
 
 
 def decode_out(arr: np.ndarray, out: str) -> np.ndarray:

@@ -91,6 +91,22 @@ def test_grouped_argument_errors(fg):
     assert L.fg_k_grouped_fp8_gemm_tn_contiguous(2, 128, 256, 256, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None) == -1
 
 
+def test_fp4_argument_errors(fg):
+    L = fg.lib
+    # packed FP4 B must start on a 32-byte boundary (16 is not enough); the FP8 rules hold too
+    assert L.fg_fp8_fp4_gemm_nt(128, 256, 512, FAKE, FAKE, FAKE + 16, FAKE, None, FAKE, 0, None) == -1
+    assert L.fg_fp8_fp4_gemm_nt(128, 256, 200, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -1
+    assert L.fg_fp8_fp4_gemm_nt(128, 256, 512, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == -2
+    assert L.fg_fp8_fp4_gemm_nt(0, 256, 512, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0, None) == 0
+    assert L.fg_m_grouped_fp8_fp4_gemm_nt_contiguous(128, 256, 128, 2, FAKE, FAKE, FAKE + 16, FAKE, FAKE, FAKE, 0,
+                                                     None) == -1
+    assert L.fg_m_grouped_fp8_fp4_gemm_nt_contiguous(100, 256, 128, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0,
+                                                     None) == -1
+    assert L.fg_m_grouped_fp8_fp4_gemm_nt_masked(2, 64, 256, 128, FAKE, FAKE, FAKE + 16, FAKE, FAKE, 0, FAKE, 0,
+                                                 None) == -1
+    assert L.fg_m_grouped_fp8_fp4_gemm_nt_masked(2, 64, 256, 128, FAKE, FAKE, FAKE, FAKE, None, 0, FAKE, 0, None) == -1
+
+
 def test_no_device_fails_loudly(fg):
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
