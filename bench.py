@@ -55,7 +55,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 KERNEL_SOURCES = ["fg_gemm_kernel.cuh", "fg_ptx.cuh", "fg_gemm_inst.cuh", "fg_gemm_nt.cu", "fg_gemm_split.cu",
-                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_sepc.cu", "fg_gemm_dense.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh", "fg_mqa.cu"]
+                  "fg_gemm_tn.cu", "fg_gemm_layouts.cu", "fg_gemm_sepc.cu", "fg_gemm_dense.cu", "fg_gemm_swiglu.cu", "fg_fp8.cuh", "fg_mqa.cu",
+                  "fg_gemm_fp4.cu", "fg_gemm_fp4_grouped.cu"]
 
 
 def align4(x: int) -> int:
@@ -168,6 +169,15 @@ class DensePair:
                    "A 1x128 / B 128x128 UE8M0 scales; FP32 C accumulated into FP32 D")
     SHAPES = [("prefill", 4096, 7168, 2048), ("decode", 64, 7168, 4096)]
     WITH_C = True        # FP32 C accumulated into an FP32 D (else no C and a BF16 D)
+    PREFIX = ""          # kernel-name prefix in the per-kernel table
+
+    @staticmethod
+    def make_weights(torch, fg, xb, n, k):
+        """E4M3 weights with one scale per 128x128 block (the library's quantiser)."""
+        b = torch.empty((n, k), dtype=torch.uint8, device="cuda")
+        sfb = torch.zeros((1, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
+        fg.quantize_128x128_blocks(xb, b, sfb)
+        return b, sfb[0]
 
     def __init__(self, torch, fg, seed):
         import workloads
@@ -179,17 +189,15 @@ class DensePair:
             c = workloads.device_normal(seed + 10 * i + 2, (m, n)) if self.WITH_C else None
             a = torch.empty((m, k), dtype=torch.uint8, device="cuda")
             sfa = torch.zeros((cdiv(k, 512), align4(m)), dtype=torch.int32, device="cuda")
-            b = torch.empty((n, k), dtype=torch.uint8, device="cuda")
-            sfb = torch.zeros((1, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
             fg.quantize_1x128_rows(xa, a, sfa)
-            fg.quantize_128x128_blocks(xb, b, sfb)
+            b, sfb = self.make_weights(torch, fg, xb, n, k)
             del xa, xb
             d = torch.empty((m, n), dtype=torch.float32 if self.WITH_C else torch.bfloat16, device="cuda")
             flops = 2.0 * m * n * k
-            nbytes = (m * k + n * k + sfa.numel() * 4 + sfb.numel() * 4 + (m * n * 4 if self.WITH_C else 0)
+            nbytes = (m * k + b.numel() + sfa.numel() * 4 + sfb.numel() * 4 + (m * n * 4 if self.WITH_C else 0)
                       + m * n * d.element_size())
-            self.parts.append({"name": nm, "m": m, "n": n, "k": k, "a": a, "sfa": sfa, "b": b, "sfb": sfb[0],
-                               "c": c, "d": d, "flops": flops, "bytes": nbytes})
+            self.parts.append({"name": self.PREFIX + nm, "m": m, "n": n, "k": k, "a": a, "sfa": sfa, "b": b,
+                               "sfb": sfb, "c": c, "d": d, "flops": flops, "bytes": nbytes})
         torch.cuda.synchronize()
 
     def launches(self):
@@ -276,21 +284,28 @@ class Contiguous:
         del xa
         pad = torch.from_numpy(np.nonzero(row_token < 0)[0]).cuda()
         self.a[pad] = workloads.device_bytes(seed + 2, (len(pad), k))
-        self.b = torch.empty((g, n, k), dtype=torch.uint8, device="cuda")
-        self.sfb = torch.zeros((g, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
-        for e in range(g):
-            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
-            fg.quantize_128x128_blocks(xb, self.b[e:e + 1], self.sfb[e:e + 1])
+        self.b, self.sfb = self.make_expert_weights(torch, fg, seed, g, n, k)
         self.m_indices = torch.from_numpy(m_indices).cuda()
         self.d = torch.empty((m_total, n), dtype=torch.bfloat16, device="cuda")
         nv = int(counts.sum())
         used = int((counts > 0).sum())
         self.nv, self.used = nv, used
         self.flops = 2.0 * nv * n * k
-        self.bytes = (nv * k + used * n * k + self.sfa.numel() * 4 + self.sfb.numel() * 4 + nv * n * 2
+        self.bytes = (nv * k + used * self.b[0].numel() + self.sfb.numel() * 4 + self.sfa.numel() * 4 + nv * n * 2
                       + m_total * 4)
-        self.parts = [{"name": "contiguous", "flops": self.flops, "bytes": self.bytes}]
+        self.parts = [{"name": self.name, "flops": self.flops, "bytes": self.bytes}]
         torch.cuda.synchronize()
+
+    @staticmethod
+    def make_expert_weights(torch, fg, seed, g, n, k):
+        """Per expert: N(0, 0.02^2) draws, E4M3 with one scale per 128x128 block."""
+        import workloads
+        b = torch.empty((g, n, k), dtype=torch.uint8, device="cuda")
+        sfb = torch.zeros((g, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
+        for e in range(g):
+            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
+            fg.quantize_128x128_blocks(xb, b[e:e + 1], sfb[e:e + 1])
+        return b, sfb
 
     def launches(self):
         return [lambda: self.fg.m_grouped_fp8_gemm_nt_contiguous(self.a, self.sfa, self.b, self.sfb,
@@ -306,6 +321,7 @@ class Masked:
     name = "masked"
     description = ("M-grouped masked FP8 NT GEMM: 32 experts x 256 rows, masked_m ~ U{0..256} on the device, "
                    "N=4096 K=2048, BF16 D")
+    FP4 = False
 
     def __init__(self, torch, fg, seed):
         import numpy as np
@@ -321,24 +337,21 @@ class Masked:
             if mm[e] < m_max:
                 self.a[e, mm[e]:] = workloads.device_bytes(seed + 50 + e, (m_max - mm[e], k))
         del x
-        self.b = torch.empty((g, n, k), dtype=torch.uint8, device="cuda")
-        self.sfb = torch.zeros((g, cdiv(k, 512), align4(cdiv(n, 128))), dtype=torch.int32, device="cuda")
-        for e in range(g):
-            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
-            fg.quantize_128x128_blocks(xb, self.b[e:e + 1], self.sfb[e:e + 1])
+        self.b, self.sfb = Contiguous.make_expert_weights(torch, fg, seed, g, n, k) if not self.FP4 \
+            else Fp4Contiguous.make_expert_weights(torch, fg, seed, g, n, k)
         self.masked_m = torch.from_numpy(mm).cuda()
         self.d = torch.empty((g, m_max, n), dtype=torch.bfloat16, device="cuda")
         nv = int(mm.sum())
         used = int((mm > 0).sum())
         self.flops = 2.0 * nv * n * k
-        self.bytes = nv * k + used * n * k + nv * n * 2 + self.sfa.numel() * 4 + self.sfb.numel() * 4
-        self.parts = [{"name": "masked", "flops": self.flops, "bytes": self.bytes}]
+        self.bytes = nv * k + used * self.b[0].numel() + nv * n * 2 + self.sfa.numel() * 4 + self.sfb.numel() * 4
+        self.parts = [{"name": self.name, "flops": self.flops, "bytes": self.bytes}]
         self.expected_m = int(mm.mean())
         torch.cuda.synchronize()
 
     def launches(self):
-        return [lambda: self.fg.m_grouped_fp8_gemm_nt_masked(self.a, self.sfa, self.b, self.sfb, self.masked_m,
-                                                             self.d, expected_m=self.expected_m)]
+        f = self.fg.m_grouped_fp8_fp4_gemm_nt_masked if self.FP4 else self.fg.m_grouped_fp8_gemm_nt_masked
+        return [lambda: f(self.a, self.sfa, self.b, self.sfb, self.masked_m, self.d, expected_m=self.expected_m)]
 
     def e2e_io(self):
         ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.masked_m)]
@@ -461,6 +474,66 @@ class Quant:
         outs = [(t, self.torch.empty_like(t, device="cpu").pin_memory())
                 for _nm, _f, _x, q, sf in self.items for t in (q, sf)]
         return ins, outs
+
+
+class Fp4DensePair(DensePair):
+    """The dense pair with FP4 weights (the FP8 x FP4 GEMM): B quantised by the library's
+    MXFP4 quantiser to E2M1 codes with one UE8M0 scale per 32 K elements of a row."""
+    name = "fp4_dense_pair"
+    description = ("dense FP8 x FP4 NT GEMM pair: prefill M=4096 N=7168 K=2048 + decode M=64 N=7168 K=4096; "
+                   "A 1x128 UE8M0, B E2M1 with 1x32 UE8M0 scales; FP32 C accumulated into FP32 D")
+    PREFIX = "fp4_"
+
+    @staticmethod
+    def make_weights(torch, fg, xb, n, k):
+        b = torch.empty((n, k // 2), dtype=torch.uint8, device="cuda")
+        sfb = torch.zeros((k // 128, align4(n)), dtype=torch.int32, device="cuda")
+        fg.quantize_mxfp4(xb, b, sfb)
+        return b, sfb
+
+    def launches(self):
+        return [lambda p=p: self.fg.fp8_fp4_gemm_nt(p["a"], p["sfa"], p["b"], p["sfb"], p["d"], c=p["c"])
+                for p in self.parts]
+
+
+class Fp4Prefill(Fp4DensePair):
+    name = "fp4_prefill"
+    description = "dense FP8 x FP4 NT GEMM M=4096 N=7168 K=2048, FP32 C accumulated into FP32 D"
+    SHAPES = [("prefill", 4096, 7168, 2048)]
+
+
+class Fp4Decode(Fp4DensePair):
+    name = "fp4_decode"
+    description = "dense FP8 x FP4 NT GEMM M=64 N=7168 K=4096, FP32 C accumulated into FP32 D"
+    SHAPES = [("decode", 64, 7168, 4096)]
+
+
+class Fp4Contiguous(Contiguous):
+    name = "fp4_contiguous"
+    description = ("M-grouped contiguous FP8 x FP4 NT GEMM: the contiguous configuration (32 experts, N=4096 "
+                   "K=4096, BF16 D) with E2M1 expert weights and 1x32 UE8M0 scales")
+
+    @staticmethod
+    def make_expert_weights(torch, fg, seed, g, n, k):
+        """Per expert: N(0, 0.02^2) draws, MXFP4 by the library's quantiser."""
+        import workloads
+        b = torch.empty((g, n, k // 2), dtype=torch.uint8, device="cuda")
+        sfb = torch.zeros((g, k // 128, align4(n)), dtype=torch.int32, device="cuda")
+        for e in range(g):
+            xb = workloads.device_normal(seed + 100 + e, (1, n, k), std=0.02)
+            fg.quantize_mxfp4(xb, b[e:e + 1], sfb[e:e + 1])
+        return b, sfb
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_fp4_gemm_nt_contiguous(self.a, self.sfa, self.b, self.sfb,
+                                                                     self.m_indices, self.d)]
+
+
+class Fp4Masked(Masked):
+    name = "fp4_masked"
+    description = ("M-grouped masked FP8 x FP4 NT GEMM: the masked configuration (32 experts x 256 rows, N=4096 "
+                   "K=2048, BF16 D) with E2M1 expert weights and 1x32 UE8M0 scales")
+    FP4 = True
 
 
 class _PrefillLayout(Prefill):
@@ -586,12 +659,14 @@ class ContiguousNN(Contiguous):
 
 
 WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, Quant, PrefillNN,
-                                 PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits)}
+                                 PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits, Fp4DensePair,
+                                 Fp4Prefill, Fp4Decode, Fp4Contiguous, Fp4Masked)}
 
 # The benchmark configurations beside the headline pair (recorded in config.kernels of
 # the default run): (configuration number, workload).
 # (configuration number, or the scope row for the quantisers, which no configuration names)
-OTHER_CONFIGS = [(0, "small"), (2, "contiguous"), (3, "masked"), (4, "k_grouped"), ("NEXT-1", "quant")]
+OTHER_CONFIGS = [(0, "small"), (2, "contiguous"), (3, "masked"), (4, "k_grouped"), ("NEXT-1", "quant"),
+                 ("NEXT-4", "fp4_dense_pair"), ("NEXT-4", "fp4_contiguous"), ("NEXT-4", "fp4_masked")]
 NOMINAL_HBM_GBS = 8000.0        # the stated HBM roof (about 8 TB/s)
 NOMINAL_FP8_TFLOPS = 4500.0     # the stated dense FP8 tensor roof (about 4.5 PFLOP/s)
 MIN_TIMED_SECONDS = 0.5         # repeat the --steps pass until the timed region lasts this long

@@ -295,6 +295,14 @@ int fg_quantize_128x128_blocks(int G, int N, int K, const float* w, uint8_t* q, 
 int fg_quantize_1x128_cols(int K, int MN, const float* x, uint8_t* q, int32_t* sf,
                            fg_stream_t stream);
 
+/* w [G][N][K] FP32 -> q [G][N][K/2] packed E2M1 (element 2i in bits 0-3 of byte i) and
+ * sf [G][K/128][align4(N)] int32: the FP4 weights of the FP8 x FP4 GEMMs, one UE8M0 scale
+ * per 32 K elements of a row, four per word.  Scale of a block: the smallest power of two
+ * 2^e with amax <= 6 * 2^e (byte e + 127, clamped to [0, 254]; an all-zero block gets 127);
+ * code: E2M1 round-to-nearest-even of x * 2^-e (ties to the even mantissa).  K % 128 == 0;
+ * every word of sf's [K/128][N] part is written, its padding words are not. */
+int fg_quantize_mxfp4(int G, int N, int K, const float* w, uint8_t* q, int32_t* sf, fg_stream_t stream);
+
 /*
  * MQA logits of the lightning indexer, non-paged (docsearch section 11 "Use V3.2 MQA
  * Kernels for Indexers", fp8_mqa_logits): for query token i and every kv token j in

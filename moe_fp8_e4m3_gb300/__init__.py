@@ -43,6 +43,7 @@ _SIGNATURES = {
     "fg_quantize_1x128_rows": (_I, [_I, _I, _P, _P, _P, _P]),
     "fg_quantize_128x128_blocks": (_I, [_I, _I, _I, _P, _P, _P, _P]),
     "fg_quantize_1x128_cols": (_I, [_I, _I, _P, _P, _P, _P]),
+    "fg_quantize_mxfp4": (_I, [_I, _I, _I, _P, _P, _P, _P]),
     "fg_get_mk_alignment_for_contiguous_layout": (_I, []),
     "fg_get_tma_aligned_size": (_I, [_I, _I]),
     "fg_set_num_sms": (None, [_I]),
@@ -305,6 +306,14 @@ def quantize_128x128_blocks(w, q, sf, stream=None) -> None:
     g, n, k = (1, *w.shape) if w.dim() == 2 else w.shape
     _check(lib.fg_quantize_128x128_blocks(g, n, k, _ptr(w), _ptr(q), _ptr(sf), _stream(stream)),
            "quantize_128x128_blocks")
+
+
+def quantize_mxfp4(w, q, sf, stream=None) -> None:
+    """w [G,N,K] (or [N,K]) FP32 -> q [.., N, K/2] packed E2M1, sf [G, K/128, align4(N)]
+    (one UE8M0 scale per 32 K elements of a row): the FP4 weights of the FP8 x FP4 GEMMs."""
+    _f32(w, "w"); _fp4(q, "q"); _i32(sf, "sf")
+    g, n, k = (1, *w.shape) if w.dim() == 2 else w.shape
+    _check(lib.fg_quantize_mxfp4(g, n, k, _ptr(w), _ptr(q), _ptr(sf), _stream(stream)), "quantize_mxfp4")
 
 
 def quantize_1x128_cols(x, q, sf, stream=None) -> None:

@@ -13,6 +13,11 @@
 // clamped to [0, 254]; an all-zero group gets byte 127).  Code: E4M3
 // round-to-nearest-even of x * 2^-e, which is exact scaling and never exceeds 448.
 // All three kernels are HBM-bound streaming passes: one read of x, one write of q.
+//
+// A fourth kernel makes the weights of the FP8 x FP4 GEMMs ("FP4 with UE8M0 SF", the
+// Chinese post's "Mega MoE" section): E2M1 codes with one UE8M0 scale per 32 K elements
+// of a row (the MXFP4 block), the smallest power of two 2^e with amax <= 6 * 2^e.
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -70,6 +75,49 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float* __restrict
     const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
     const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
     if (lane == 0) sf[(long long)w * sf_ld + row] = static_cast<int32_t>(byte | b1 << 8 | b2 << 16 | b3 << 24);
+}
+
+// MXFP4 scale exponent: the smallest e with amax <= 6 * 2^e.  With amax = fr * 2^ex,
+// fr in [0.5, 1): amax / 2^(ex-3) = 8 fr lies in [4, 8), within 6 iff fr <= 0.75.
+__device__ __forceinline__ int mxfp4_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int ex;
+    const float fr = frexpf(amax, &ex);
+    int e = fr <= 0.75f ? ex - 3 : ex - 2;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// One warp per (row, 128-wide K-group): lane l holds K elements 4l..4l+3, eight lanes per
+// 32-wide block.  The eight warps of a CTA take eight consecutive rows of one K-group, so
+// their scale words are adjacent.  Codes: E2M1 round-to-nearest-even of x * 2^-e (exact
+// scaling; never above 6), element 2i in bits 0-3 of byte i.
+__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const float* __restrict__ w, long long rows, int N,
+                                                          int K, uint8_t* __restrict__ q, int32_t* __restrict__ sf,
+                                                          int sf_ld) {
+    const int kgs = K / 128;
+    const int kg = static_cast<int>(blockIdx.x % kgs);
+    const long long row = (long long)(blockIdx.x / kgs) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const float4 t = __ldg(reinterpret_cast<const float4*>(w + row * K + kg * 128) + lane);
+    float amax = fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w)));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = mxfp4_exponent(amax);
+    const float v[4] = {ldexpf(t.x, -e), ldexpf(t.y, -e), ldexpf(t.z, -e), ldexpf(t.w, -e)};
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        codes |= (static_cast<uint32_t>(__nv_cvt_float_to_fp4(v[i], __NV_E2M1, cudaRoundNearest)) & 0xFu) << (4 * i);
+    *reinterpret_cast<uint16_t*>(q + row * (K / 2) + kg * 64 + lane * 2) = static_cast<uint16_t>(codes);
+    const uint32_t byte = static_cast<uint32_t>(e + 127);
+    const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
+    const uint32_t b2 = __shfl_sync(0xffffffffu, byte, 16);
+    const uint32_t b3 = __shfl_sync(0xffffffffu, byte, 24);
+    if (lane == 0) {
+        const long long g = row / N, n = row % N;
+        sf[(g * kgs + kg) * sf_ld + n] = static_cast<int32_t>(byte | b1 << 8 | b2 << 16 | b3 << 24);
+    }
 }
 
 // The scale byte of K-group kg goes straight into its packed word (byte kg mod 4); the CTA
@@ -221,6 +269,19 @@ int fg_quantize_128x128_blocks(int G, int N, int K, const float* w, uint8_t* q, 
     if (nblk > 65535) return FG_ERR_INVALID_ARG;
     quant_blocks_kernel<<<dim3(K / 128, nblk, G), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         w, N, K, q, sf, align4(nblk), kp);
+    return finish_launch();
+}
+
+int fg_quantize_mxfp4(int G, int N, int K, const float* w, uint8_t* q, int32_t* sf, fg_stream_t stream) {
+    if (G < 1 || N < 1 || K < 128 || K % 128 != 0 || !w || !q || !sf || !al16(w) || !al16(q) || !al16(sf))
+        return FG_ERR_INVALID_ARG;
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return FG_ERR_CUDA; }
+    const long long rows = (long long)G * N;
+    const long long blocks = (rows + 7) / 8 * (K / 128);
+    if (blocks > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
+    quant_mxfp4_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w, rows, N, K, q, sf, align4(N));
     return finish_launch();
 }
 
