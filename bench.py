@@ -584,10 +584,10 @@ class ContiguousSwiGLU(Contiguous):
         m_total, inter = self.a.shape[0], self.b.shape[1] // 2
         self.q = torch.empty((m_total, inter), dtype=torch.uint8, device="cuda")
         self.sfq = torch.zeros((cdiv(inter, 512), align4(m_total)), dtype=torch.int32, device="cuda")
-        k, n2, nv = self.a.shape[1], self.b.shape[1], self.nv
-        self.bytes = (nv * k + self.used * n2 * k + self.sfa.numel() * 4 + self.sfb.numel() * 4
+        k, nv = self.a.shape[1], self.nv
+        self.bytes = (nv * k + self.used * self.b[0].numel() + self.sfa.numel() * 4 + self.sfb.numel() * 4
                       + nv * inter + nv * (inter // 128) + m_total * 4)
-        self.parts = [{"name": "contiguous_swiglu", "flops": self.flops, "bytes": self.bytes}]
+        self.parts = [{"name": self.name, "flops": self.flops, "bytes": self.bytes}]
         del self.d
         torch.cuda.synchronize()
 
@@ -598,6 +598,20 @@ class ContiguousSwiGLU(Contiguous):
     def e2e_io(self):
         ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.m_indices)]
         return ins, [(t, self.torch.empty_like(t, device="cpu").pin_memory()) for t in (self.q, self.sfq)]
+
+
+class Fp4ContiguousSwiGLU(ContiguousSwiGLU):
+    """The fused gate-up GEMM with FP4 expert weights (the Mega MoE's linear 1 in FP8 x FP4,
+    then SwiGLU and the requantisation for linear 2)."""
+    name = "fp4_contiguous_swiglu"
+    description = ("M-grouped contiguous FP8 x FP4 gate-up GEMM with fused SwiGLU + per-1x128 E4M3 "
+                   "requantisation: the contiguous_swiglu configuration with E2M1 expert weights and 1x32 "
+                   "UE8M0 scales")
+    make_expert_weights = staticmethod(Fp4Contiguous.make_expert_weights)
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(self.a, self.sfa, self.b, self.sfb,
+                                                                            self.m_indices, self.q, self.sfq)]
 
 
 class MqaLogits:
@@ -660,7 +674,7 @@ class ContiguousNN(Contiguous):
 
 WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, Quant, PrefillNN,
                                  PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits, Fp4DensePair,
-                                 Fp4Prefill, Fp4Decode, Fp4Contiguous, Fp4Masked)}
+                                 Fp4Prefill, Fp4Decode, Fp4Contiguous, Fp4Masked, Fp4ContiguousSwiGLU)}
 
 # The benchmark configurations beside the headline pair (recorded in config.kernels of
 # the default run): (configuration number, workload).

@@ -264,6 +264,21 @@ int fg_m_grouped_fp8_fp4_gemm_nt_masked(int G, int M_max, int N, int K,
                                         const uint8_t* b, const int32_t* sfb,
                                         const int32_t* masked_m, int expected_m,
                                         void* d, int d_dtype, fg_stream_t stream);
+/* The fused gate-up GEMMs with FP4 weights (the Mega MoE's linear 1 in FP8 x FP4, then
+ * SwiGLU and the requantisation for linear 2): fg_m_grouped_fp8_gemm_nt_{contiguous,
+ * masked}_swiglu with b [G][2I][K/2] packed E2M1 (I gate rows, then I up rows) and
+ * sfb [G][K/128][align4(2I)] (one scale per 32 K elements of a row); everything else,
+ * q and sfq included, as for the E4M3-weight calls.  b must be 32-byte aligned. */
+int fg_m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G,
+                                                   const uint8_t* a, const int32_t* sfa,
+                                                   const uint8_t* b, const int32_t* sfb,
+                                                   const int32_t* m_indices, uint8_t* q, int32_t* sfq,
+                                                   fg_stream_t stream);
+int fg_m_grouped_fp8_fp4_gemm_nt_masked_swiglu(int G, int M_max, int I, int K,
+                                               const uint8_t* a, const int32_t* sfa,
+                                               const uint8_t* b, const int32_t* sfb,
+                                               const int32_t* masked_m, uint8_t* q, int32_t* sfq,
+                                               fg_stream_t stream);
 
 /*
  * FP32 -> E4M3 quantisation with UE8M0 scales, written straight into the packed,

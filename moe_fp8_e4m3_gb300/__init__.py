@@ -39,6 +39,8 @@ _SIGNATURES = {
     "fg_fp8_fp4_gemm_nt": (_I, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_fp4_gemm_nt_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P]),
     "fg_m_grouped_fp8_fp4_gemm_nt_masked": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P]),
+    "fg_m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fg_m_grouped_fp8_fp4_gemm_nt_masked_swiglu": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_k_grouped_fp8_gemm_tn_contiguous": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "fg_quantize_1x128_rows": (_I, [_I, _I, _P, _P, _P, _P]),
     "fg_quantize_128x128_blocks": (_I, [_I, _I, _I, _P, _P, _P, _P]),
@@ -269,6 +271,33 @@ def m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, masked_m, d, expected_m=0, 
     _check(lib.fg_m_grouped_fp8_fp4_gemm_nt_masked(g, m_max, n, k, _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb),
                                                    _ptr(masked_m), int(expected_m), _ptr(d), code,
                                                    _stream(stream)), "m_grouped_fp8_fp4_gemm_nt_masked")
+
+
+def m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(a, sfa, b, sfb, m_indices, q, sfq, stream=None) -> None:
+    """The fused gate-up GEMM with FP4 weights.  a [M_total,K]; b [G,2I,K/2] packed E2M1 (I gate
+    rows, then I up rows); sfb [G, K/128, align4(2I)] int32 (1x32 blocks); q [M_total,I] uint8
+    (out); sfq [ceil(I/512), align4(M_total)] int32 (out)."""
+    _fp8(a, "a"); _fp4(b, "b"); _fp8(q, "q"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _i32(sfq, "sfq")
+    _i32(m_indices, "m_indices")
+    m_total, k = a.shape
+    g, n2, _ = b.shape
+    _check(lib.fg_m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(m_total, n2 // 2, k, g, _ptr(a), _ptr(sfa), _ptr(b),
+                                                              _ptr(sfb), _ptr(m_indices), _ptr(q), _ptr(sfq),
+                                                              _stream(stream)),
+           "m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu")
+
+
+def m_grouped_fp8_fp4_gemm_nt_masked_swiglu(a, sfa, b, sfb, masked_m, q, sfq, stream=None) -> None:
+    """The masked fused gate-up GEMM with FP4 weights.  a [G,M_max,K]; b [G,2I,K/2] packed E2M1;
+    sfb [G, K/128, align4(2I)]; q [G,M_max,I] uint8 (out); sfq [G, ceil(I/512), align4(M_max)]."""
+    _fp8(a, "a"); _fp4(b, "b"); _fp8(q, "q"); _i32(sfa, "sfa"); _i32(sfb, "sfb"); _i32(sfq, "sfq")
+    _i32(masked_m, "masked_m")
+    g, m_max, k = a.shape
+    n2 = b.shape[1]
+    _check(lib.fg_m_grouped_fp8_fp4_gemm_nt_masked_swiglu(g, m_max, n2 // 2, k, _ptr(a), _ptr(sfa), _ptr(b),
+                                                          _ptr(sfb), _ptr(masked_m), _ptr(q), _ptr(sfq),
+                                                          _stream(stream)),
+           "m_grouped_fp8_fp4_gemm_nt_masked_swiglu")
 
 
 def k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, ks, d, c=None, stream=None) -> None:

@@ -356,21 +356,27 @@ int launch_nt(int bn, const GemmParams& p, const fg::GemmMaps& gm, int grid, cud
 }
 
 // Gate-up weights b [G][2I][K] seen as [2G halves][I rows][K]: a {128 K, 128 rows, 2 halves}
-// box brings a tile's gate rows and the matching up rows in one copy.
-bool encode_swiglu_b(CUtensorMap* map, const void* b, int K, int I, int G) {
+// box brings a tile's gate rows and the matching up rows in one copy.  fp4: b [G][2I][K/2]
+// packed E2M1, unpacked by the tensor map as for encode_b_nt.
+bool encode_swiglu_b(CUtensorMap* map, const void* b, int K, int I, int G, bool fp4) {
+    const cuuint64_t row_bytes = fp4 ? (cuuint64_t)K / 2 : (cuuint64_t)K;
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)I, (cuuint64_t)2 * G};
-    cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)I * K};
+    cuuint64_t strides[2] = {row_bytes, (cuuint64_t)I * row_bytes};
     cuuint32_t box[3] = {128, 128, 2};
     cuuint32_t elem_strides[3] = {1, 1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims, strides, box, elem_strides,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return g_encode(map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                    const_cast<void*>(b), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_swiglu(const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
-    const cudaError_t e = p.kind == fg::kMasked
-                              ? fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kMasked>(p, gm, grid, s)
-                              : fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kContiguous>(p, gm, grid, s);
+int launch_swiglu(bool fp4, const GemmParams& p, const fg::GemmMaps& gm, int grid, cudaStream_t s) {
+    const bool masked = p.kind == fg::kMasked;
+    const cudaError_t e =
+        fp4 ? (masked ? fg::launch_gemm<256, fg::kMajNTF4, false, true, false, fg::kMasked>(p, gm, grid, s)
+                      : fg::launch_gemm<256, fg::kMajNTF4, false, true, false, fg::kContiguous>(p, gm, grid, s))
+            : (masked ? fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kMasked>(p, gm, grid, s)
+                      : fg::launch_gemm<256, fg::kMajNT, false, true, false, fg::kContiguous>(p, gm, grid, s));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return FG_ERR_CUDA;
@@ -722,13 +728,18 @@ int fg_m_grouped_fp8_fp4_gemm_nt_contiguous(int M_total, int N, int K, int G, co
     return m_grouped_contiguous(false, true, M_total, N, K, G, a, sfa, b, sfb, m_indices, d, d_dtype, stream);
 }
 
-int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G, const uint8_t* a,
-                                               const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
-                                               const int32_t* m_indices, uint8_t* q, int32_t* sfq,
-                                               fg_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Gate-up GEMM + SwiGLU + requantisation, contiguous layout; fp4: B [G][2I][K/2] packed
+// E2M1 with 1x32 scales.
+int swiglu_contiguous(bool fp4, int M_total, int I, int K, int G, const uint8_t* a, const int32_t* sfa,
+                      const uint8_t* b, const int32_t* sfb, const int32_t* m_indices, uint8_t* q, int32_t* sfq,
+                      fg_stream_t stream) {
     if (M_total < 0 || M_total % 128 != 0 || G < 1 || I < 128 || I % 128 != 0) return FG_ERR_INVALID_ARG;
     const int N = 2 * I;
-    int rc = check_nt_operands(N, K, a, sfa, b, sfb, q, FG_BF16);
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, q, FG_BF16, fp4);
     if (rc) return rc;
     if (!sfq || !aligned4(sfq) || !m_indices || !aligned4(m_indices)) return FG_ERR_INVALID_ARG;
     if ((long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
@@ -742,8 +753,8 @@ int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G,
     p.M = M_total; p.N = N; p.K = K; p.G = G;
     p.num_mb = M_total / 128; p.num_nb = I / 128;
     p.sfa = sfa; p.sfb = sfb;
-    p.sfa_ld = align4(M_total); p.sfb_ld = align4(ceil_div(N, 128));
-    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    p.sfa_ld = align4(M_total);
+    set_b_scales(p, N, K, fp4);
     p.sfa_rows = M_total;
     p.m_indices = m_indices;
     p.d = q;
@@ -752,24 +763,24 @@ int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G,
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
     if (!encode_2d(&gm.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, M_total, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_swiglu_b(&gm.b, b, K, I, G) ||
+        !encode_swiglu_b(&gm.b, b, K, I, G, fp4) ||
         !encode_2d(&gm.d, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, I, M_total, I, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)p.num_mb * p.num_nb;
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
-        std::fprintf(stderr, "[fg] m_grouped_contiguous_swiglu M_total=%d I=%d K=%d G=%d grid=%d\n", M_total, I, K, G, grid);
-    return launch_swiglu(p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+        std::fprintf(stderr, "[fg] m_grouped_%scontiguous_swiglu M_total=%d I=%d K=%d G=%d grid=%d\n",
+                     fp4 ? "fp8_fp4_" : "", M_total, I, K, G, grid);
+    return launch_swiglu(fp4, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const uint8_t* a,
-                                           const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
-                                           const int32_t* masked_m, uint8_t* q, int32_t* sfq,
-                                           fg_stream_t stream) {
+// The masked layout of swiglu_contiguous.
+int swiglu_masked(bool fp4, int G, int M_max, int I, int K, const uint8_t* a, const int32_t* sfa, const uint8_t* b,
+                  const int32_t* sfb, const int32_t* masked_m, uint8_t* q, int32_t* sfq, fg_stream_t stream) {
     if (G < 1 || G > fg::kMaxGroups || M_max < 1 || I < 128 || I % 128 != 0) return FG_ERR_INVALID_ARG;
     const int N = 2 * I;
     if ((long long)G * M_max > 0x7fffffffLL || (long long)G * N > 0x7fffffffLL) return FG_ERR_INVALID_ARG;
-    int rc = check_nt_operands(N, K, a, sfa, b, sfb, q, FG_BF16);
+    int rc = check_nt_operands(N, K, a, sfa, b, sfb, q, FG_BF16, fp4);
     if (rc) return rc;
     if (!sfq || !aligned4(sfq) || !masked_m || !aligned4(masked_m)) return FG_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
@@ -781,9 +792,9 @@ int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const
     p.M = M_max; p.N = N; p.K = K; p.G = G;
     p.num_mb = ceil_div(M_max, 128); p.num_nb = I / 128;
     p.sfa = sfa; p.sfb = sfb;
-    p.sfa_ld = align4(M_max); p.sfb_ld = align4(ceil_div(N, 128));
+    p.sfa_ld = align4(M_max);
     p.sfa_gstride = (long long)ceil_div(K, 512) * p.sfa_ld;
-    p.sfb_gstride = (long long)ceil_div(K, 512) * p.sfb_ld;
+    set_b_scales(p, N, K, fp4);
     p.sfa_rows = M_max;
     p.masked_m = masked_m;
     p.d = q;
@@ -793,14 +804,47 @@ int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const
     fg::GemmMaps gm;
     std::memset(&gm, 0, sizeof(gm));
     if (!encode_2d(&gm.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, (uint64_t)G * M_max, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_swiglu_b(&gm.b, b, K, I, G) ||
+        !encode_swiglu_b(&gm.b, b, K, I, G, fp4) ||
         !encode_2d(&gm.d, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, I, (uint64_t)G * M_max, I, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return FG_ERR_INVALID_ARG;
     const long long tiles = (long long)G * p.num_mb * p.num_nb;   // upper bound
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (print_configs())
-        std::fprintf(stderr, "[fg] m_grouped_masked_swiglu G=%d M_max=%d I=%d K=%d grid=%d\n", G, M_max, I, K, grid);
-    return launch_swiglu(p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+        std::fprintf(stderr, "[fg] m_grouped_%smasked_swiglu G=%d M_max=%d I=%d K=%d grid=%d\n",
+                     fp4 ? "fp8_fp4_" : "", G, M_max, I, K, grid);
+    return launch_swiglu(fp4, p, gm, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fg_m_grouped_fp8_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G, const uint8_t* a,
+                                               const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                               const int32_t* m_indices, uint8_t* q, int32_t* sfq,
+                                               fg_stream_t stream) {
+    return swiglu_contiguous(false, M_total, I, K, G, a, sfa, b, sfb, m_indices, q, sfq, stream);
+}
+
+int fg_m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(int M_total, int I, int K, int G, const uint8_t* a,
+                                                   const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                                   const int32_t* m_indices, uint8_t* q, int32_t* sfq,
+                                                   fg_stream_t stream) {
+    return swiglu_contiguous(true, M_total, I, K, G, a, sfa, b, sfb, m_indices, q, sfq, stream);
+}
+
+int fg_m_grouped_fp8_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const uint8_t* a,
+                                           const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                           const int32_t* masked_m, uint8_t* q, int32_t* sfq,
+                                           fg_stream_t stream) {
+    return swiglu_masked(false, G, M_max, I, K, a, sfa, b, sfb, masked_m, q, sfq, stream);
+}
+
+int fg_m_grouped_fp8_fp4_gemm_nt_masked_swiglu(int G, int M_max, int I, int K, const uint8_t* a,
+                                               const int32_t* sfa, const uint8_t* b, const int32_t* sfb,
+                                               const int32_t* masked_m, uint8_t* q, int32_t* sfq,
+                                               fg_stream_t stream) {
+    return swiglu_masked(true, G, M_max, I, K, a, sfa, b, sfb, masked_m, q, sfq, stream);
 }
 
 int fg_fp8_mqa_logits(int S, int T, int H, int D, const uint8_t* q, const uint8_t* kv, const float* kv_sf,

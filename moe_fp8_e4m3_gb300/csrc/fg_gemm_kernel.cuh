@@ -523,10 +523,10 @@ fg_gemm_kernel(const GemmParams p, const __grid_constant__ GemmMaps maps) {
     // an E4M3 row takes and the MMA walks the stage exactly as for FP8 B; the instruction
     // descriptor names E2M1 for B, and each K=32 MMA selects its own scale byte.
     constexpr bool kFp4B = (kMaj & 4) != 0;
-    static_assert(!kFp4B || (kMaj == kMajNTF4 && !kSwiGLU), "FP4 B is a K-major NT operand");
+    static_assert(!kFp4B || kMaj == kMajNTF4, "FP4 B is a K-major NT operand");
     static_assert(!(kSplit && (kMaj & 3) != kMajNT), "split-K clusters are a dense NT variant");
     static_assert(!kBmn || BN % 128 == 0, "N-major B tiles are whole 128-column swizzle atoms");
-    static_assert(!kSwiGLU || (BN == 256 && kMaj == kMajNT && !kSplit),
+    static_assert(!kSwiGLU || (BN == 256 && (kMaj & 3) == kMajNT && !kSplit),
                   "the SwiGLU epilogue pairs 128 gate and 128 up columns in one NT tile");
     static_assert(!kSepC || (!kSplit && !kSwiGLU), "C slots belong to the plain epilogue");
     static_assert(!kSwiGLU || kKindT == kContiguous || kKindT == kMasked, "the SwiGLU epilogue is an M-grouped layout");

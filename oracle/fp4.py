@@ -201,3 +201,37 @@ def m_grouped_fp8_fp4_gemm_nt_masked(a, sfa_words, b, sfb_words, masked_m, exper
         be = dequant_mxfp4(b[e], mx_scales(sfb_words[e], n, k))
         out[e] = dequant_k_major(a[e, sel], sa) @ be.T
     return out
+
+
+# ---------------------------------------------------------------------------
+# Gate-up GEMM with FP4 weights + SwiGLU + per-1x128 requantisation
+# ---------------------------------------------------------------------------
+def m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(a, sfa_words, b, sfb_words, m_indices, rows=None):
+    """The Mega MoE linear 1 in FP8 x FP4 (zh post "Mega MoE": linear 1 FP8xFP4, then SwiGLU)
+    on one GPU: the contiguous gate-up GEMM with b [G, 2I, K/2] packed E2M1 (I gate rows,
+    then I up rows; sfb_words [G][K/128][align4(2I)]), then SwiGLU and the per-1x128 E4M3
+    requantisation of ``oracle.swiglu``.  Returns (codes, scale bytes, written) as the FP8
+    form does."""
+    from .swiglu import swiglu_quantize
+    h, written = m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa_words, b, sfb_words, m_indices, rows)
+    i = b.shape[1] // 2
+    q = np.zeros((h.shape[0], i), np.uint8)
+    sf = np.zeros((h.shape[0], i // K_GROUP), np.uint8)
+    if written.any():
+        q[written], sf[written] = swiglu_quantize(h[written])
+    return q, sf, written
+
+
+def m_grouped_fp8_fp4_gemm_nt_masked_swiglu(a, sfa_words, b, sfb_words, masked_m, experts=None):
+    """The masked gate-up GEMM with FP4 weights + SwiGLU + requantisation:
+    {g: (codes [masked_m[g], I], scale bytes [masked_m[g], I/128])}."""
+    from .swiglu import swiglu_quantize
+    d = m_grouped_fp8_fp4_gemm_nt_masked(a, sfa_words, b, sfb_words, masked_m, experts)
+    out = {}
+    i = b.shape[1] // 2
+    for g, h in d.items():
+        if h.shape[0] == 0:
+            out[g] = (np.zeros((0, i), np.uint8), np.zeros((0, i // K_GROUP), np.uint8))
+        else:
+            out[g] = swiglu_quantize(h)
+    return out

@@ -537,6 +537,51 @@ def check_fp4_grouped_brute_force(seed=11):
                 assert abs(Fraction(out[e][i, j]) - ex) <= abs(ex) * Fraction(1, 2 ** 45) + Fraction(1, 2 ** 900)
 
 
+def check_fp4_swiglu_brute_force(seed=12):
+    """FP4 gate-up GEMM + SwiGLU + requantisation on a tiny case: each GEMM element exactly
+    (rationals, nibbles and 1x32 scale bytes read here), SiLU from scipy's expit, then each
+    code within half an E4M3 spacing of y / scale and each scale the smallest admissible power
+    of two; the masked form on the same weights."""
+    from scipy.special import expit
+    from oracle import fp4 as FP4
+    g = np.random.Generator(np.random.PCG64(seed))
+    num_groups, inter, k = 2, 128, 256
+    m_indices = np.array([1, -1, 0, 1], dtype=np.int32)
+    a = rand_codes(g, (len(m_indices), k))
+    b = rand_fp4(g, (num_groups, 2 * inter, k // 2))
+    sfa = rand_words(g, len(m_indices), k // 128)
+    sfb = np.stack([rand_words(g, 2 * inter, k // 32) for _ in range(num_groups)])
+    q, sf, written = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(a, sfa, b, sfb, m_indices)
+    assert list(written) == [e >= 0 for e in m_indices]
+
+    def check_row(arow_a, arow_sfa, r, e, qrow, sfrow):
+        h = np.array([float(exact_fp4_dense(arow_a, arow_sfa, b[e], sfb[e], None, r, j)) for j in range(2 * inter)])
+        y = (h[:inter] * expit(h[:inter]) * h[inter:]).astype(np.float32).astype(np.float64)
+        amax = Fraction(float(np.abs(y).max()))
+        scale = fr_ue8(int(sfrow[0]))
+        assert amax <= 448 * scale and (amax == 0 or amax > 224 * scale), (r, float(amax), int(sfrow[0]))
+        for j in range(inter):
+            t = Fraction(float(y[j])) / scale
+            code = fr_e4m3(int(qrow[j]))
+            mag = abs(t)
+            ex = max(mag.numerator.bit_length() - mag.denominator.bit_length(), -6) if mag else -6
+            if mag and Fraction(2) ** ex > mag:
+                ex -= 1
+            spacing = Fraction(2) ** (max(ex, -6) - 3)
+            assert abs(code - t) <= spacing / 2, (r, j, float(t), float(code))
+
+    for r, e in enumerate(m_indices):
+        if e >= 0:
+            check_row(a, sfa, r, e, q[r], sf[r])
+    a3 = a.reshape(2, 2, k)
+    sfa3 = np.stack([rand_words(g, 2, k // 128) for _ in range(2)])
+    out = FP4.m_grouped_fp8_fp4_gemm_nt_masked_swiglu(a3, sfa3, b, sfb, [2, 1])
+    assert out[0][0].shape == (2, inter) and out[1][0].shape == (1, inter)
+    for e in range(2):
+        for r in range(out[e][0].shape[0]):
+            check_row(a3[e], sfa3[e], r, e, out[e][0][r], out[e][1][r])
+
+
 ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_force,
               check_mqa_brute_force, check_mqa_closed_form,
               check_silu_library, check_swiglu_brute_force, check_swiglu_exact_probe,
@@ -544,4 +589,4 @@ ALL_CHECKS = [check_golden_gemm, check_dense_brute_force, check_layouts_brute_fo
               check_masked_brute_force, check_k_grouped_brute_force, check_identity,
               check_one_hot, check_scale_probe, check_integer_valued,
               check_fp4_format_golden, check_fp4_golden_gemm, check_fp4_dense_brute_force,
-              check_fp4_grouped_brute_force]
+              check_fp4_grouped_brute_force, check_fp4_swiglu_brute_force]

@@ -188,3 +188,94 @@ def test_fp4_masked_parity(fg, bn, monkeypatch):
         assert not sent[e, :mm].any() and sent[e, mm:].all(), f"group {e}: rows beyond mask written"
         if mm:
             C.compare(vals[e, :mm], ref[e], f"fp4 masked BN={bn} group {e}")
+
+
+# ----------------------------------------------- FP4 gate-up GEMM + SwiGLU
+SENT_Q = 0xAB
+SENT_W = -0x21436588
+
+
+def _y_ref(h):
+    from oracle import swiglu as S
+    return S.swiglu(h).astype(np.float32).astype(np.float64)
+
+
+def test_fp4_contiguous_swiglu_parity(fg):
+    """The Mega MoE's linear 1 in FP8 x FP4 with the fused SwiGLU + requantisation (same
+    comparison rule as the E4M3-weight form: one E4M3 spacing, >= 99 % identical codes)."""
+    from gpu_util import dev
+    from oracle import swiglu as S
+    inter = 256
+    case = C.fp4_contiguous_case(31, num_tokens=512, num_routed=16, topk=3, num_groups=5, n=2 * inter, k=384)
+    m_total = case["m_total"]
+    q = torch.full((m_total, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.full(((inter + 511) // 512, (m_total + 3) // 4 * 4), SENT_W, dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(dev(case["a"]), dev(case["sfa"]), dev(case["b"]),
+                                                   dev(case["sfb"]), dev(case["m_indices"]), q, sfq)
+    _status_ok(fg)
+    qh, sfh = q.cpu().numpy(), sfq.cpu().numpy()
+    written = case["m_indices"] >= 0
+    assert np.all(qh[~written] == SENT_Q), "padding rows of q written"
+    sf_bytes = F.unpack_ue8m0(sfh, m_total, inter // 128)
+    sent_bytes = F.unpack_ue8m0(np.full_like(sfh, SENT_W), m_total, inter // 128)
+    assert np.array_equal(sf_bytes[~written], sent_bytes[~written]), "padding rows of sfq written"
+    h, w2 = C.fp4_contiguous_ref(case)
+    assert np.array_equal(w2, written)
+    q_ref, sf_ref = S.swiglu_quantize(h[written])
+    C.compare_quantised(qh[written], sf_bytes[written], q_ref, sf_ref, _y_ref(h[written]), "fp4 contiguous swiglu")
+    q_o, sf_o, _ = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                                  case["m_indices"])
+    assert np.array_equal(q_o[written], q_ref) and np.array_equal(sf_o[written], sf_ref)
+
+
+def test_fp4_masked_swiglu_parity(fg):
+    from gpu_util import dev
+    inter = 384
+    masks = [0, 1, 129, 200, 64, 33]
+    case = C.fp4_masked_case(32, num_groups=len(masks), m_max=200, n=2 * inter, k=256, masked_m=masks)
+    g_, m_max = case["g"], case["m_max"]
+    q = torch.full((g_, m_max, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.full((g_, (inter + 511) // 512, (m_max + 3) // 4 * 4), SENT_W, dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_masked_swiglu(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                               dev(case["masked_m"]), q, sfq)
+    _status_ok(fg)
+    qh, sfh = q.cpu().numpy(), sfq.cpu().numpy()
+    ref = FP4.m_grouped_fp8_fp4_gemm_nt_masked_swiglu(case["a"], case["sfa"], case["b"], case["sfb"],
+                                                     case["masked_m"])
+    hs = C.fp4_masked_ref(case)
+    for e in range(g_):
+        mm = int(case["masked_m"][e])
+        assert np.all(qh[e, mm:] == SENT_Q), f"group {e}: rows beyond the mask written"
+        sb = F.unpack_ue8m0(sfh[e], m_max, inter // 128)
+        sent = F.unpack_ue8m0(np.full_like(sfh[e], SENT_W), m_max, inter // 128)
+        assert np.array_equal(sb[mm:], sent[mm:]), f"group {e}: scale bytes beyond the mask written"
+        if mm:
+            C.compare_quantised(qh[e, :mm], sb[:mm], ref[e][0], ref[e][1], _y_ref(hs[e]),
+                                f"fp4 masked swiglu group {e}")
+
+
+def test_fp4_swiglu_exact_probe_bit_exact(fg):
+    """A[m, 0] in {1, 2}, the rest 0; gate row i has one code g_i in {4, 6} (scale 2^4: 64
+    or 96), up row i one code in {-2, -1, 0, 1, 2, 3}: the GEMM is exact and SiLU(gate) ==
+    gate in FP32 and FP64 (gate >= 64), so codes and scales must be identical."""
+    from gpu_util import dev
+    g = np.random.Generator(np.random.PCG64(33))
+    inter, k, m_total = 256, 128, 256
+    a = np.zeros((m_total, k), np.uint8)
+    a[:, 0] = np.where(g.integers(0, 2, m_total) == 0, 0x38, 0x40)
+    codes = np.zeros((1, 2 * inter, k), np.uint8)
+    codes[0, :inter, 0] = np.array([0x6, 0x7], np.uint8)[g.integers(0, 2, inter)]            # 4, 6
+    codes[0, inter:, 0] = np.array([0xC, 0xA, 0x0, 0x2, 0x4, 0x5], np.uint8)[g.integers(0, 6, inter)]
+    b = FP4.pack_fp4(codes)
+    sb = np.full((2 * inter, k // 32), 127, np.uint8)
+    sb[:inter, 0] = 131                                                                        # gate x 16
+    sfa = F.pack_ue8m0(np.full((m_total, 1), 127, np.uint8))
+    sfb = FP4.pack_mx_scales(sb)[None]
+    m_indices = np.zeros(m_total, np.int32)
+    q = torch.full((m_total, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.zeros((1, (m_total + 3) // 4 * 4), dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(dev(a), dev(sfa), dev(b), dev(sfb), dev(m_indices), q, sfq)
+    _status_ok(fg)
+    q_ref, sf_ref, _ = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(a, sfa, b, sfb, m_indices)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(F.unpack_ue8m0(sfq.cpu().numpy(), m_total, inter // 128), sf_ref)
