@@ -440,12 +440,13 @@ class Small(DensePair):
 
 class Quant:
     """The quantise/pack kernels on operands of the benchmark GEMMs' sizes: 1x128 row groups
-    of an activation x[8192, 7168], 128x128 blocks of a weight w[7168, 2048], and 1x128
-    groups along K of a K-grouped operand x[16384, 4096].  HBM-bound streams: one FP32 read,
-    one E4M3 write and the packed scale words."""
+    of an activation x[8192, 7168], 128x128 blocks of a weight w[7168, 2048], 1x128 groups
+    along K of a K-grouped operand x[16384, 4096], and MXFP4 (E2M1, 1x32 scales) of the
+    expert weights w[32 x 4096, 4096].  HBM-bound streams: one FP32 read, one code write
+    and the packed scale words."""
     name = "quant"
     description = ("FP32 -> E4M3 + packed UE8M0 quantisation: 1x128 rows of [8192, 7168], 128x128 "
-                   "blocks of [7168, 2048], 1x128 columns of [16384, 4096]")
+                   "blocks of [7168, 2048], 1x128 columns of [16384, 4096]; FP32 -> MXFP4 of [32 x 4096, 4096]")
 
     def __init__(self, torch, fg, seed):
         import workloads
@@ -453,6 +454,7 @@ class Quant:
         rows_x = workloads.device_normal(seed, (8192, 7168))
         blk_w = workloads.device_normal(seed + 1, (7168, 2048))
         col_x = workloads.device_normal(seed + 2, (16384, 4096))
+        mx_w = workloads.device_normal(seed + 3, (32 * 4096, 4096), std=0.02)
         u8, i32 = torch.uint8, torch.int32
         self.items = [
             ("quant_rows", fg.quantize_1x128_rows, rows_x, torch.empty((8192, 7168), dtype=u8, device="cuda"),
@@ -461,6 +463,8 @@ class Quant:
              torch.zeros((1, cdiv(2048, 512), align4(cdiv(7168, 128))), dtype=i32, device="cuda")),
             ("quant_cols", fg.quantize_1x128_cols, col_x, torch.empty((16384, 4096), dtype=u8, device="cuda"),
              torch.zeros((cdiv(16384, 512), align4(4096)), dtype=i32, device="cuda")),
+            ("quant_mxfp4", fg.quantize_mxfp4, mx_w, torch.empty((32 * 4096, 2048), dtype=u8, device="cuda"),
+             torch.zeros((4096 // 128, align4(32 * 4096)), dtype=i32, device="cuda")),
         ]
         self.parts = [{"name": nm, "flops": 0.0, "bound": "hbm",
                        "bytes": x.numel() * 4 + q.numel() + sf.numel() * 4} for nm, _f, x, q, sf in self.items]

@@ -52,7 +52,8 @@ def dense_ref(case, rows=None):
 
 
 # ------------------------------------------------------------- contiguous
-def contiguous_case(seed, **kw):
+def contiguous_case(seed, weights="fp8", **kw):
+    """weights: "fp8" (E4M3, 128x128-block scales) or "fp4" (packed E2M1, 1x32 scales)."""
     w = workloads.contiguous(seed, **kw)
     m_indices = w["m_indices"]
     m_total = len(m_indices)
@@ -64,13 +65,17 @@ def contiguous_case(seed, **kw):
     a[valid] = qa
     sa[valid] = qsa
     g_count, n, _ = w["b"].shape
-    bq = np.empty((g_count, n, k), np.uint8)
-    sfb = []
-    for e in range(g_count):
-        bq[e], sb = F.quantize_blocks(w["b"][e])
-        sfb.append(F.pack_ue8m0(sb))
+    if weights == "fp4":
+        bq, sfb = _mxfp4_experts(w["b"])
+    else:
+        bq = np.empty((g_count, n, k), np.uint8)
+        sfb = []
+        for e in range(g_count):
+            bq[e], sb = F.quantize_blocks(w["b"][e])
+            sfb.append(F.pack_ue8m0(sb))
+        sfb = np.stack(sfb)
     return {"m_total": m_total, "n": n, "k": k, "g": g_count, "a": a, "sfa": F.pack_ue8m0(sa),
-            "b": bq, "sfb": np.stack(sfb), "m_indices": m_indices, "counts": w["counts"]}
+            "b": bq, "sfb": sfb, "m_indices": m_indices, "counts": w["counts"]}
 
 
 def contiguous_ref(case, rows=None):
@@ -79,7 +84,8 @@ def contiguous_ref(case, rows=None):
 
 
 # ----------------------------------------------------------------- masked
-def masked_case(seed, **kw):
+def masked_case(seed, weights="fp8", **kw):
+    """weights: "fp8" (E4M3, 128x128-block scales) or "fp4" (packed E2M1, 1x32 scales)."""
     w = workloads.masked(seed, **kw)
     g_count, m_max, k = w["x"].shape
     n = w["b"].shape[1]
@@ -95,10 +101,15 @@ def masked_case(seed, **kw):
             a[e, :mm] = qa
             sa[:mm] = qsa
         sfa.append(F.pack_ue8m0(sa))
-        bq[e], sb = F.quantize_blocks(w["b"][e])
-        sfb.append(F.pack_ue8m0(sb))
+        if weights != "fp4":
+            bq[e], sb = F.quantize_blocks(w["b"][e])
+            sfb.append(F.pack_ue8m0(sb))
+    if weights == "fp4":
+        bq, sfb = _mxfp4_experts(w["b"])
+    else:
+        sfb = np.stack(sfb)
     return {"g": g_count, "m_max": m_max, "n": n, "k": k, "a": a, "sfa": np.stack(sfa), "b": bq,
-            "sfb": np.stack(sfb), "masked_m": w["masked_m"]}
+            "sfb": sfb, "masked_m": w["masked_m"]}
 
 
 def masked_ref(case, experts=None, rows=None):
@@ -146,10 +157,7 @@ def fp4_dense_ref(case, rows=None):
 
 def fp4_contiguous_case(seed, **kw):
     """The contiguous routing and activations of :func:`contiguous_case` with MXFP4 weights."""
-    w = workloads.contiguous(seed, **kw)
-    case = contiguous_case(seed, **kw)
-    case["b"], case["sfb"] = _mxfp4_experts(w["b"])
-    return case
+    return contiguous_case(seed, weights="fp4", **kw)
 
 
 def fp4_contiguous_ref(case, rows=None):
@@ -159,10 +167,7 @@ def fp4_contiguous_ref(case, rows=None):
 
 def fp4_masked_case(seed, **kw):
     """The masked activations of :func:`masked_case` with MXFP4 weights."""
-    w = workloads.masked(seed, **kw)
-    case = masked_case(seed, **kw)
-    case["b"], case["sfb"] = _mxfp4_experts(w["b"])
-    return case
+    return masked_case(seed, weights="fp4", **kw)
 
 
 def fp4_masked_ref(case, experts=None, rows=None):

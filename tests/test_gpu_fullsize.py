@@ -149,3 +149,88 @@ def test_mqa_logits_full_size(fg):
     got = run(fg, case, True)
     rows = _rows(4096, 24, 9)
     check(case, got, True, rows=rows)
+
+
+# ------------------------------------------------------------------ FP8 x FP4
+def test_fp4_prefill_full_size(fg):
+    """The FP8 x FP4 prefill 4096 x 7168 x 2048 with FP32 C (MXFP4 weights); the decode shape
+    is compared in full by the FP4 parity tests."""
+    from gpu_util import GuardedOut, dev
+    m, n, k = 4096, 7168, 2048
+    case = C.fp4_dense_case(1011, m, n, k, True, "f32")
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_fp4_gemm_nt(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), out.tensor,
+                       c=dev(case["c"]))
+    _ok(fg)
+    out.check_guards()
+    got = out.values()
+    assert np.all(np.isfinite(got))
+    rows = _rows(m, 48, 12)
+    C.compare(got[rows], C.fp4_dense_ref(case, rows=rows), "fp4 prefill sampled rows")
+
+
+def test_fp4_contiguous_full_size(fg):
+    from gpu_util import GuardedOut, dev
+    case = C.fp4_contiguous_case(1012)        # 8192 tokens, top-6 of 256, experts 0-31, N=K=4096
+    d = GuardedOut(case["m_total"], case["n"], "bf16")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                            dev(case["m_indices"]), d.tensor)
+    _ok(fg)
+    d.check_guards()
+    written = case["m_indices"] >= 0
+    assert np.array_equal(~d.is_sentinel(), written), "padding rows written or valid rows missing"
+    vals = d.values()
+    assert np.all(np.isfinite(vals[written]))
+    g = np.random.Generator(np.random.PCG64(13))
+    rows = np.sort(g.choice(np.nonzero(written)[0], size=48, replace=False))
+    ref, _ = C.fp4_contiguous_ref(case, rows=rows)
+    C.compare(vals[rows], ref, "fp4 contiguous sampled rows")
+
+
+def test_fp4_masked_full_size(fg):
+    from gpu_util import GuardedOut, dev
+    case = C.fp4_masked_case(1013)            # 32 experts x 256 rows, N=4096, K=2048
+    g_, m_max, n = case["g"], case["m_max"], case["n"]
+    d = GuardedOut(g_ * m_max, n, "bf16")
+    fg.m_grouped_fp8_fp4_gemm_nt_masked(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]),
+                                        dev(case["masked_m"]), d.tensor.view(g_, m_max, n),
+                                        expected_m=int(np.mean(case["masked_m"])))
+    _ok(fg)
+    d.check_guards()
+    sent = d.is_sentinel().reshape(g_, m_max)
+    vals = d.values().reshape(g_, m_max, n)
+    g = np.random.Generator(np.random.PCG64(14))
+    rows = {}
+    for e in range(g_):
+        mm = int(case["masked_m"][e])
+        assert not sent[e, :mm].any() and sent[e, mm:].all(), f"group {e}: rows beyond the mask written"
+        assert np.all(np.isfinite(vals[e, :mm]))
+        pick = set(g.choice(mm, size=min(mm, 6), replace=False).tolist()) if mm > 0 else set()
+        rows[e] = np.array(sorted(pick | ({0, mm - 1} if mm > 0 else set())), dtype=np.int64)
+    ref = C.fp4_masked_ref(case, rows=rows)
+    for e in range(g_):
+        C.compare(vals[e, rows[e]], ref[e], f"fp4 masked group {e} sampled rows")
+
+
+def test_fp4_contiguous_swiglu_full_size(fg):
+    """The fused gate-up GEMM with FP4 weights at the contiguous benchmark shape
+    (B [32, 2 x 2048, 4096] packed E2M1): sampled valid rows, every padding row untouched."""
+    from gpu_util import dev
+    from oracle import swiglu as S
+    from test_gpu_swiglu import SENT_Q, _sf_bytes, _y_ref, compare_quantised
+    case = C.fp4_contiguous_case(1014)
+    m_total, inter = case["m_total"], case["n"] // 2
+    q = torch.full((m_total, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.zeros(((inter + 511) // 512, (m_total + 3) // 4 * 4), dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(dev(case["a"]), dev(case["sfa"]), dev(case["b"]),
+                                                   dev(case["sfb"]), dev(case["m_indices"]), q, sfq)
+    _ok(fg)
+    qh = q.cpu().numpy()
+    written = case["m_indices"] >= 0
+    assert np.all(qh[~written] == SENT_Q), "padding rows written"
+    g = np.random.Generator(np.random.PCG64(15))
+    rows = np.sort(g.choice(np.nonzero(written)[0], size=48, replace=False))
+    h, _ = C.fp4_contiguous_ref(case, rows=rows)
+    q_ref, sf_ref = S.swiglu_quantize(h)
+    sf = _sf_bytes(sfq.cpu().numpy(), m_total, inter // 128)[rows]
+    compare_quantised(qh[rows], sf, q_ref, sf_ref, _y_ref(h), "fp4 contiguous swiglu full size")

@@ -96,3 +96,38 @@ def test_k_grouped_choice(fg, capfd, monkeypatch):
     fg.k_grouped_fp8_gemm_tn_contiguous(_u8(k_total, m), _i32(_cdiv(k_total, 512), _a4(m)), _u8(k_total, n),
                                         _i32(_cdiv(k_total, 512), _a4(n)), ks, c, c=c)
     assert int(_printed(capfd, "k_grouped_tn")["BN"]) == 128
+
+
+def _fp4_dense(fg, m, n, k):
+    a, sfa = _u8(m, k), _i32(_cdiv(k, 512), _a4(m))
+    b, sfb = _u8(n, k // 2), _i32(k // 128, _a4(n))
+    d = torch.zeros((m, n), dtype=torch.float32, device="cuda")
+    fg.fp8_fp4_gemm_nt(a, sfa, b, sfb, d, c=torch.zeros((m, n), dtype=torch.float32, device="cuda"))
+
+
+@pytest.mark.parametrize("m,n,k,bn,split", [
+    (4096, 7168, 2048, 224, 1),    # the prefill shape with FP4 weights
+    (64, 7168, 4096, 128, 2),      # the decode shape with FP4 weights
+])
+def test_fp4_dense_choices(fg, capfd, monkeypatch, m, n, k, bn, split):
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    _fp4_dense(fg, m, n, k)
+    cfg = _printed(capfd, "fp8_fp4_gemm_nt")
+    assert (int(cfg["BN"]), int(cfg["split"])) == (bn, split), cfg
+
+
+def test_fp4_grouped_choices(fg, capfd, monkeypatch):
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    g, m_total, n, k = 32, 8192, 4096, 4096
+    m_indices = (torch.arange(m_total, device="cuda", dtype=torch.int32) // 256).contiguous()
+    d = torch.zeros((m_total, n), dtype=torch.bfloat16, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous(_u8(m_total, k), _i32(_cdiv(k, 512), _a4(m_total)), _u8(g, n, k // 2),
+                                            _i32(g, k // 128, _a4(n)), m_indices, d)
+    assert int(_printed(capfd, "m_grouped_fp8_fp4_nt_contiguous")["BN"]) == 224
+    m_max, k2 = 256, 2048
+    masked_m = torch.full((g,), 128, dtype=torch.int32, device="cuda")
+    d2 = torch.zeros((g, m_max, n), dtype=torch.bfloat16, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_masked(_u8(g, m_max, k2), _i32(g, _cdiv(k2, 512), _a4(m_max)), _u8(g, n, k2 // 2),
+                                        _i32(g, k2 // 128, _a4(n)), masked_m, d2, expected_m=128)
+    assert int(_printed(capfd, "m_grouped_fp8_fp4_masked")["BN"]) == 224
+
