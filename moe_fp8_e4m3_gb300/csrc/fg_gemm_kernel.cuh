@@ -16,6 +16,12 @@
 // K-groups; it is copied to TMEM unchanged and the MMA's scale-factor byte selector
 // picks byte (g mod 4).
 //
+// FP8 x FP4 (operand-major bit 2): B holds E2M1 codes, two per byte, with one UE8M0 scale
+// per 32 K elements of a row.  The tensor map unpacks B into the padded shared-memory form
+// of a sub-byte MMA operand (the same bytes per stage as E4M3 B), the instruction
+// descriptor names E2M1 for B, B's scale word changes every K-group (its four bytes are
+// the K-group's four 32-wide blocks), and each K=32 MMA selects its own B byte.
+//
 // Warp roles (320 threads):
 //   warps 0, 8  TMA producers of A tiles into a ring of shared-memory stages (even / odd
 //               stages)
