@@ -104,3 +104,37 @@ def test_k_grouped_single_expert_owns_k(fg, alias):
     C.compare(vals[0], ref[0], "k-grouped expert 0, K = 16384, wide-range scales")
     for e in range(1, g_):
         assert np.array_equal(vals[e].astype(np.float32), w["c"][e]), f"expert {e}: D != C"
+
+
+# ------------------------------------------------------------------ FP8 x FP4
+def wide_fp4_case(seed, m, n, k, with_c, out):
+    """The wide-range draws with the weights quantised to MXFP4 (E2M1, one scale per 32 K
+    elements of a row), so B's scales vary per row and 32-wide block as well."""
+    from oracle import fp4 as FP4
+    w = workloads.dense_wide_range(seed, m, n, k, with_c)
+    a, sa = F.quantize_rows(w["a"])
+    b, sb = FP4.quantize_mxfp4(w["b"])
+    assert int(sa.max()) - int(sa.min()) >= 18 and int(sb.max()) - int(sb.min()) >= 18
+    return {"m": m, "n": n, "k": k, "a": a, "sfa": F.pack_ue8m0(sa), "b": b, "sfb": FP4.pack_mx_scales(sb),
+            "c": w["c"], "out": out}
+
+
+@pytest.mark.parametrize("form", ["default", "one_cta", "split4"])
+@pytest.mark.parametrize("m,n", [(256, 512), (64, 1024)])
+def test_fp4_k16384_wide_range(fg, form, m, n, monkeypatch):
+    """The FP8 x FP4 GEMM at K = 16384 with falling wide-range magnitudes: the scales of both
+    operands are applied per 32-wide K step inside the tensor core and the FP32 accumulator
+    holds the whole K loop, in every dense launch form."""
+    from gpu_util import GuardedOut, dev
+    if form == "one_cta":
+        monkeypatch.setenv("FG_FORCE_SPLIT", "1")
+    elif form == "split4":
+        monkeypatch.setenv("FG_FORCE_SPLIT", "4")
+    case = wide_fp4_case(4250 + m, m, n, K_LONG, True, "f32")
+    got = GuardedOut(m, n, "f32")
+    fg.fp8_fp4_gemm_nt(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), got.tensor,
+                       c=dev(case["c"]))
+    _ok(fg)
+    got.check_guards()
+    ref = oracle.fp8_fp4_gemm_nt(case["a"], case["sfa"], case["b"], case["sfb"], case["c"])
+    C.compare(got.values(), ref, f"fp4 {m}x{n}x{K_LONG} wide-range scales ({form})")
