@@ -321,7 +321,7 @@ class Masked:
     name = "masked"
     description = ("M-grouped masked FP8 NT GEMM: 32 experts x 256 rows, masked_m ~ U{0..256} on the device, "
                    "N=4096 K=2048, BF16 D")
-    FP4 = False
+    make_expert_weights = staticmethod(Contiguous.make_expert_weights)
 
     def __init__(self, torch, fg, seed):
         import numpy as np
@@ -337,8 +337,7 @@ class Masked:
             if mm[e] < m_max:
                 self.a[e, mm[e]:] = workloads.device_bytes(seed + 50 + e, (m_max - mm[e], k))
         del x
-        self.b, self.sfb = Contiguous.make_expert_weights(torch, fg, seed, g, n, k) if not self.FP4 \
-            else Fp4Contiguous.make_expert_weights(torch, fg, seed, g, n, k)
+        self.b, self.sfb = self.make_expert_weights(torch, fg, seed, g, n, k)
         self.masked_m = torch.from_numpy(mm).cuda()
         self.d = torch.empty((g, m_max, n), dtype=torch.bfloat16, device="cuda")
         nv = int(mm.sum())
@@ -350,8 +349,8 @@ class Masked:
         torch.cuda.synchronize()
 
     def launches(self):
-        f = self.fg.m_grouped_fp8_fp4_gemm_nt_masked if self.FP4 else self.fg.m_grouped_fp8_gemm_nt_masked
-        return [lambda: f(self.a, self.sfa, self.b, self.sfb, self.masked_m, self.d, expected_m=self.expected_m)]
+        return [lambda: self.fg.m_grouped_fp8_gemm_nt_masked(self.a, self.sfa, self.b, self.sfb, self.masked_m,
+                                                             self.d, expected_m=self.expected_m)]
 
     def e2e_io(self):
         ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.masked_m)]
@@ -537,7 +536,11 @@ class Fp4Masked(Masked):
     name = "fp4_masked"
     description = ("M-grouped masked FP8 x FP4 NT GEMM: the masked configuration (32 experts x 256 rows, N=4096 "
                    "K=2048, BF16 D) with E2M1 expert weights and 1x32 UE8M0 scales")
-    FP4 = True
+    make_expert_weights = staticmethod(Fp4Contiguous.make_expert_weights)
+
+    def launches(self):
+        return [lambda: self.fg.m_grouped_fp8_fp4_gemm_nt_masked(self.a, self.sfa, self.b, self.sfb, self.masked_m,
+                                                                 self.d, expected_m=self.expected_m)]
 
 
 class _PrefillLayout(Prefill):
