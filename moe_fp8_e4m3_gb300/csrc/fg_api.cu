@@ -206,7 +206,9 @@ int forced_split() {
 // MMAs: it is charged 15 % more, and with a heavy epilogue (a C, or an FP32 D: 4 bytes per
 // output) it is not considered.  Measured on GB300: 4096 x 7168 x 2048 FP32 D without C,
 // BN=224 67 us against BN=256 74 us; BF16 D, masked 32 x 256 x 4096 x 2048 62.1 us against
-// 63.9 us and contiguous 32 x 4096 x 4096 137.9 us against 140.2 us.
+// 63.9 us and contiguous 32 x 4096 x 4096 137.9 us against 140.2 us.  Where two widths cost
+// the same, the order of the list decides: the same GEMM with an FP32 C (7 waves of 224 or 8
+// of 192) ran 76.6 us at BN=224, 80.3 us at 192 and 82.0 us at 128.
 // The FP8 x FP4 variants exist at two widths, 128 and 224 (fp4 restricts the choice to them).
 bool fp4_width(int bn) { return bn == 128 || bn == 224; }
 
