@@ -621,6 +621,54 @@ class Fp4ContiguousSwiGLU(ContiguousSwiGLU):
                                                                             self.m_indices, self.q, self.sfq)]
 
 
+class MoeMlp(ContiguousSwiGLU):
+    """The MoE expert MLP of the contiguous configuration on one GPU: linear 1 (gate-up, I =
+    2048, K = 4096) with the fused SwiGLU + E4M3 requantisation, then linear 2 (the down
+    projection, [32, 4096, 2048] weights) on its output, BF16 D.  One step = both GEMMs."""
+    name = "moe_mlp"
+    description = ("MoE expert MLP, contiguous layout (32 experts, top-6 of 8192 tokens): gate-up GEMM with fused "
+                   "SwiGLU + E4M3 requantisation (I=2048, K=4096), then the down projection (N=4096, K=2048), BF16 D")
+
+    def __init__(self, torch, fg, seed):
+        super().__init__(torch, fg, seed)
+        g, inter = self.b.shape[0], self.q.shape[1]
+        hidden = self.a.shape[1]
+        self.w2, self.sfw2 = self.make_expert_weights(torch, fg, seed + 5000, g, hidden, inter)
+        m_total = self.a.shape[0]
+        self.d = torch.empty((m_total, hidden), dtype=torch.bfloat16, device="cuda")
+        nv = self.nv
+        down_flops = 2.0 * nv * hidden * inter
+        down_bytes = (nv * inter + self.sfq.numel() * 4 + self.used * self.w2[0].numel() + self.sfw2.numel() * 4
+                      + nv * hidden * 2 + m_total * 4)
+        self.parts = [self.parts[0], {"name": self.name + "_down", "flops": down_flops, "bytes": down_bytes}]
+        torch.cuda.synchronize()
+
+    def down(self):
+        self.fg.m_grouped_fp8_gemm_nt_contiguous(self.q, self.sfq, self.w2, self.sfw2, self.m_indices, self.d)
+
+    def launches(self):
+        return super().launches() + [self.down]
+
+    def e2e_io(self):
+        ins = [(t, t.cpu().pin_memory()) for t in (self.a, self.sfa, self.b, self.sfb, self.w2, self.sfw2,
+                                                     self.m_indices)]
+        return ins, [(self.d, self.torch.empty_like(self.d, device="cpu").pin_memory())]
+
+
+class Fp4MoeMlp(MoeMlp):
+    """The MoE expert MLP with FP4 (MXFP4) weights in both GEMMs."""
+    name = "fp4_moe_mlp"
+    description = ("MoE expert MLP in FP8 x FP4: the moe_mlp configuration with E2M1 expert weights and 1x32 "
+                   "UE8M0 scales in both GEMMs")
+    make_expert_weights = staticmethod(Fp4Contiguous.make_expert_weights)
+
+    def launches(self):
+        return Fp4ContiguousSwiGLU.launches(self) + [self.down]
+
+    def down(self):
+        self.fg.m_grouped_fp8_fp4_gemm_nt_contiguous(self.q, self.sfq, self.w2, self.sfw2, self.m_indices, self.d)
+
+
 class MqaLogits:
     """Lightning-indexer MQA logits (non-paged): 4096 query tokens x 4096 kv tokens, causal
     ranges (token i sees kv [0, i]), 64 heads, D = 128, clean_logits; FP32 out [4096, 4096].
@@ -681,7 +729,8 @@ class ContiguousNN(Contiguous):
 
 WORKLOADS = {w.name: w for w in (DensePair, Prefill, Decode, Small, Contiguous, Masked, KGrouped, KGroupedSeparate, Quant, PrefillNN,
                                  PrefillTN, PrefillTT, ContiguousNN, ContiguousSwiGLU, MqaLogits, Fp4DensePair,
-                                 Fp4Prefill, Fp4Decode, Fp4Contiguous, Fp4Masked, Fp4ContiguousSwiGLU)}
+                                 Fp4Prefill, Fp4Decode, Fp4Contiguous, Fp4Masked, Fp4ContiguousSwiGLU, MoeMlp,
+                                 Fp4MoeMlp)}
 
 # The benchmark configurations beside the headline pair (recorded in config.kernels of
 # the default run): (configuration number, workload).

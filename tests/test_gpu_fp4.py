@@ -279,3 +279,35 @@ def test_fp4_swiglu_exact_probe_bit_exact(fg):
     q_ref, sf_ref, _ = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(a, sfa, b, sfb, m_indices)
     assert np.array_equal(q.cpu().numpy(), q_ref)
     assert np.array_equal(F.unpack_ue8m0(sfq.cpu().numpy(), m_total, inter // 128), sf_ref)
+
+
+def test_fp4_moe_expert_chain(fg):
+    """The Mega MoE expert computation in FP8 x FP4 on one GPU: linear 1 (gate-up, FP4
+    weights) with the fused SwiGLU + E4M3 requantisation, its output consumed as is by
+    linear 2 (the down projection, FP4 weights).  Linear 1's codes are checked against the
+    oracle's, and linear 2 against the oracle GEMM on the codes linear 1 produced."""
+    from gpu_util import GuardedOut, dev
+    from oracle import swiglu as S
+    inter, hidden = 256, 384
+    case = C.fp4_contiguous_case(35, num_tokens=256, num_routed=8, topk=2, num_groups=3, n=2 * inter, k=256)
+    m_total = case["m_total"]
+    q = torch.zeros((m_total, inter), dtype=torch.uint8, device="cuda")
+    sfq = torch.zeros(((inter + 511) // 512, (m_total + 3) // 4 * 4), dtype=torch.int32, device="cuda")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous_swiglu(dev(case["a"]), dev(case["sfa"]), dev(case["b"]),
+                                                   dev(case["sfb"]), dev(case["m_indices"]), q, sfq)
+    _status_ok(fg)
+    written = case["m_indices"] >= 0
+    h, _ = C.fp4_contiguous_ref(case)
+    q_ref, sf_ref = S.swiglu_quantize(h[written])
+    qh, sfh = q.cpu().numpy(), sfq.cpu().numpy()
+    C.compare_quantised(qh[written], F.unpack_ue8m0(sfh, m_total, inter // 128)[written], q_ref, sf_ref,
+                        _y_ref(h[written]), "fp4 linear 1")
+    gw = np.random.Generator(np.random.PCG64(36))
+    w2, sfw2 = C._mxfp4_experts(gw.standard_normal((3, hidden, inter)) * 0.05)
+    d = GuardedOut(m_total, hidden, "bf16")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous(q, sfq, dev(w2), dev(sfw2), dev(case["m_indices"]), d.tensor)
+    _status_ok(fg)
+    d.check_guards()
+    ref, _ = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous(qh, sfh, w2, sfw2, case["m_indices"])
+    assert np.array_equal(~d.is_sentinel(), written)
+    C.compare(d.values()[written], ref[written], "fp4 linear 2 on linear 1's output")
