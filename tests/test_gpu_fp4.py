@@ -311,3 +311,46 @@ def test_fp4_moe_expert_chain(fg):
     ref, _ = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous(qh, sfh, w2, sfw2, case["m_indices"])
     assert np.array_equal(~d.is_sentinel(), written)
     C.compare(d.values()[written], ref[written], "fp4 linear 2 on linear 1's output")
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+def test_fp4_scale_selection_probe_split_k(fg, split, monkeypatch, capfd):
+    """The bit-exact scale probe under split-K clusters: each CTA's share of the 6 K-groups
+    starts at its own K-group (uneven shares at 4), so both the A word (four K-groups) and
+    the B word (one K-group) of its first stage come from mid-array; partial sums of powers
+    of two stay exact."""
+    from gpu_util import GuardedOut, dev
+    monkeypatch.setenv("FG_FORCE_SPLIT", split)
+    monkeypatch.setenv("FG_PRINT_CONFIGS", "1")
+    m, n, k = 64, 384, 768
+    sa = (126 + (np.arange(m)[:, None] + np.arange(k // 128)[None, :]) % 3).astype(np.uint8)
+    sb = (124 + (np.arange(n)[:, None] + 3 * np.arange(k // 32)[None, :]) % 7).astype(np.uint8)
+    a = np.full((m, k), 0x38, np.uint8)
+    b = np.full((n, k // 2), 0x22, np.uint8)
+    out = GuardedOut(m, n, "f32")
+    fg.fp8_fp4_gemm_nt(dev(a), dev(F.pack_ue8m0(sa)), dev(b), dev(FP4.pack_mx_scales(sb)), out.tensor)
+    _status_ok(fg)
+    assert _launched(capfd, "fp8_fp4_gemm_nt")["split"] == split
+    want = 32.0 * (np.repeat(np.exp2(sa - 127.0), 4, axis=1) @ np.exp2(sb - 127.0).T)
+    assert np.array_equal(out.values(), want)
+
+
+def test_fp4_contiguous_empty_groups_and_all_padding_block(fg):
+    """Expert 1 receives no tokens and the last block is all padding: with FP4 weights the
+    written rows and their values match the oracle and nothing else is written."""
+    from gpu_util import GuardedOut, dev
+    import oracle_pins as P
+    g = np.random.Generator(np.random.PCG64(37))
+    m_indices = np.array([0] * 130 + [-1] * 126 + [2] * 128 + [-1] * 128, np.int32)
+    k, n, groups = 256, 128, 3
+    a = P.rand_codes(g, (len(m_indices), k))
+    b = P.rand_fp4(g, (groups, n, k // 2))
+    sfa = P.rand_words(g, len(m_indices), k // 128)
+    sfb = np.stack([P.rand_words(g, n, k // 32) for _ in range(groups)])
+    d = GuardedOut(len(m_indices), n, "bf16")
+    fg.m_grouped_fp8_fp4_gemm_nt_contiguous(dev(a), dev(sfa), dev(b), dev(sfb), dev(m_indices), d.tensor)
+    _status_ok(fg)
+    d.check_guards()
+    ref, written = FP4.m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, m_indices)
+    assert np.array_equal(~d.is_sentinel(), written)
+    C.compare(d.values()[written], ref[written], "fp4 contiguous edge")
