@@ -23,4 +23,20 @@ __device__ __forceinline__ uint32_t e4m3(float v) {
     return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
+// 2^-e as a float, built from its exponent bits: an exact multiplier for e in [-127, 126]
+// (a finite amax gives e <= 120; the clamp only keeps the bits valid).  x * 2^-e equals
+// the scaling x / 2^e exactly wherever the result is a normal float.
+__device__ __forceinline__ float pow2_neg(int e) {
+    e = e > 126 ? 126 : e;
+    return __int_as_float((127 - e) << 23);
+}
+
+// Four already-scaled values to E4M3 (saturating, round to nearest even) in one word, the
+// first in the low byte; the values go through the paired conversion two at a time.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return (lo & 0xFFFFu) | (hi & 0xFFFFu) << 16;
+}
+
 }  // namespace fg

@@ -29,7 +29,8 @@
 
 namespace {
 
-using fg::e4m3;
+using fg::e4m3x4;
+using fg::pow2_neg;
 using fg::scale_exponent;
 
 // One warp per (row, packed word): 512 consecutive K elements, 16 per lane, 8 lanes per
@@ -61,14 +62,11 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float* __restrict
     const int e = scale_exponent(amax);
     const uint32_t byte = active ? static_cast<uint32_t>(e + 127) : 0u;
     if (active) {
+        const float sc = pow2_neg(e);
         uint32_t packed[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) word |= e4m3(ldexpf(v[4 * i + j], -e)) << (8 * j);
-            packed[i] = word;
-        }
+        for (int i = 0; i < 4; ++i)
+            packed[i] = e4m3x4(v[4 * i] * sc, v[4 * i + 1] * sc, v[4 * i + 2] * sc, v[4 * i + 3] * sc);
         *reinterpret_cast<uint4*>(q + (long long)row * K + k0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
     const uint32_t b1 = __shfl_sync(0xffffffffu, byte, 8);
@@ -172,15 +170,13 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restri
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
     const int e = scale_exponent(amax);
+    const float sc = pow2_neg(e);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         const int row = nb * 128 + warp * 16 + r;
-        if (row < N) {
-            uint32_t b = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) b |= e4m3(ldexpf(v[r][i], -e)) << (8 * i);
-            *reinterpret_cast<uint32_t*>(qbase + (long long)row * K + kg * 128 + lane * 4) = b;
-        }
+        if (row < N)
+            *reinterpret_cast<uint32_t*>(qbase + (long long)row * K + kg * 128 + lane * 4) =
+                e4m3x4(v[r][0] * sc, v[r][1] * sc, v[r][2] * sc, v[r][3] * sc);
     }
     if (threadIdx.x == 0)
         put_scale_byte(reinterpret_cast<uint8_t*>(sf + ((long long)g * kp + kg / 4) * sf_ld + nb), kg, K / 128, e);
@@ -232,14 +228,13 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const float* __restrict
     __syncthreads();
     uint8_t* dst = q + (long long)kg * 128 * MN + c0;
     if (4 * g4 < ncols) {
-        const int e0 = ex[4 * g4], e1 = ex[4 * g4 + 1], e2 = ex[4 * g4 + 2], e3 = ex[4 * g4 + 3];
+        const float s0 = pow2_neg(ex[4 * g4]), s1 = pow2_neg(ex[4 * g4 + 1]);
+        const float s2 = pow2_neg(ex[4 * g4 + 2]), s3 = pow2_neg(ex[4 * g4 + 3]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = r0 + 8 * i;
             const float4 v = reinterpret_cast<const float4*>(tile + r * kColTile)[g4];
-            *reinterpret_cast<uint32_t*>(dst + (long long)r * MN + 4 * g4) =
-                e4m3(ldexpf(v.x, -e0)) | e4m3(ldexpf(v.y, -e1)) << 8 | e4m3(ldexpf(v.z, -e2)) << 16 |
-                e4m3(ldexpf(v.w, -e3)) << 24;
+            *reinterpret_cast<uint32_t*>(dst + (long long)r * MN + 4 * g4) = e4m3x4(v.x * s0, v.y * s1, v.z * s2, v.w * s3);
         }
     }
 }
