@@ -25,7 +25,8 @@
  *     of 4 (16 bytes).  Padding entries are ignored.
  *   - A scales are one per row per K-group (1x128).  B scales of the NT calls are
  *     one per 128x128 block (MN index = n / 128); the K-grouped call takes 1x128
- *     scales along K for both operands.
+ *     scales along K for both operands; the FP8 x FP4 calls (below) take packed E2M1 B
+ *     with one scale per 32 K elements of a row.
  *   - C is optional FP32 and is accepted only with an FP32 D.  D may alias C (the same
  *     pointer: in-place accumulation, D += A @ B^T; the kernels then read no C of their own
  *     and add the product onto D with TMA reduce-adds, one FP32 add per element performed
