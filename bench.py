@@ -214,6 +214,28 @@ class DensePair:
             outs.append((p["d"], self.torch.empty_like(p["d"], device="cpu").pin_memory()))
         return ins, outs
 
+    def e2e_double(self):
+        """Two device sets of every operand and output, for the double-buffered end-to-end
+        loop: returns (bind(k), [(inputs, outputs) of set 0, of set 1]).  bind(k) points the
+        launches at set k; both sets copy from and to the same pinned host buffers."""
+        keys_in = ("a", "sfa", "b", "sfb", "c")
+        sets = [{}, {}]
+        io = [([], []), ([], [])]
+        for j, p in enumerate(self.parts):
+            host_in = {key: p[key].cpu().pin_memory() for key in keys_in if p[key] is not None}
+            host_out = self.torch.empty_like(p["d"], device="cpu").pin_memory()
+            for k in (0, 1):
+                dev = {key: (p[key] if k == 0 else (p[key].clone() if p[key] is not None else None))
+                       for key in keys_in + ("d",)}
+                sets[k][j] = dev
+                io[k][0].extend((dev[key], host_in[key]) for key in keys_in if dev[key] is not None)
+                io[k][1].append((dev["d"], host_out))
+
+        def bind(k):
+            for j, p in enumerate(self.parts):
+                p.update(sets[k][j])
+        return bind, io
+
     _oracle_inputs = None
 
     @classmethod
@@ -988,41 +1010,84 @@ def run_gpu(args):
 
     # ---- end to end through the public API with host buffers
     # Every step copies its inputs host -> device (pinned), runs the GEMMs and reads the
-    # results back device -> host.  The read-back of step i runs on a second stream while
-    # step i+1's inputs go in (the two directions use separate copy engines); step i+1's
-    # GEMMs wait for step i's read-back (they overwrite D) and step i+1's input copies wait
-    # for step i's GEMMs (stream order).  Time: first input copy to last read-back, / steps.
+    # results back device -> host; the two directions use separate copy engines.
     # (Spreading the input copies over several streams measured no faster: the host link,
     # not one DMA queue, sets the input rate.)
-    ins, outs = wl.e2e_io()
-    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
-    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
     e2e_steps = max(3, min(args.steps, 50))
     out_stream = torch.cuda.Stream()
-    out_done = None
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    for i in range(e2e_steps + 2):
-        if i == 2:
-            stream.wait_stream(out_stream)
-            t_start.record(stream)
-        for dt, ht in ins:
-            dt.copy_(ht, non_blocking=True)
-        if out_done is not None:
-            stream.wait_event(out_done)
-        for fn in launches:
-            fn()
-        computed = torch.cuda.Event()
-        computed.record(stream)
-        out_stream.wait_event(computed)
-        with torch.cuda.stream(out_stream):
-            for dt, ht in outs:
-                ht.copy_(dt, non_blocking=True)
-            out_done = torch.cuda.Event()
-            out_done.record(out_stream)
-    stream.wait_event(out_done)
-    t_end.record(stream)
-    torch.cuda.synchronize()
+    if hasattr(wl, "e2e_double"):
+        # Double-buffered: step i uses device set i % 2, so step i+1's input copies (their own
+        # stream) run beside step i's GEMMs and step i-1's read-back; a set is refilled only
+        # after the GEMMs of the step that used it two steps before, and its D is overwritten
+        # only after that step's read-back.  Time: step 2's first input copy to the last
+        # read-back, / steps.
+        bind, io = wl.e2e_double()
+        ins, outs = io[0]
+        in_stream = torch.cuda.Stream()
+        comp = [None, None]
+        out_done = [None, None]
+        for i in range(e2e_steps + 2):
+            k = i % 2
+            if comp[k] is not None:
+                in_stream.wait_event(comp[k])
+            if i == 2:
+                t_start.record(in_stream)
+            with torch.cuda.stream(in_stream):
+                for dt, ht in io[k][0]:
+                    dt.copy_(ht, non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(in_stream)
+            stream.wait_event(landed)
+            if out_done[k] is not None:
+                stream.wait_event(out_done[k])
+            bind(k)
+            for fn in launches:
+                fn()
+            comp[k] = torch.cuda.Event()
+            comp[k].record(stream)
+            out_stream.wait_event(comp[k])
+            with torch.cuda.stream(out_stream):
+                for dt, ht in io[k][1]:
+                    ht.copy_(dt, non_blocking=True)
+                out_done[k] = torch.cuda.Event()
+                out_done[k].record(out_stream)
+        t_end.record(out_stream)
+        torch.cuda.synchronize()
+        bind(0)
+        e2e_overlap = ("double-buffered device inputs and outputs: step i+1's host-to-device copies run "
+                       "beside step i's GEMMs and step i-1's device-to-host read-back")
+    else:
+        # Step i's read-back runs on a second stream while step i+1's inputs go in; step
+        # i+1's GEMMs wait for step i's read-back (they overwrite D) and step i+1's input
+        # copies wait for step i's GEMMs (stream order).
+        ins, outs = wl.e2e_io()
+        out_done = None
+        for i in range(e2e_steps + 2):
+            if i == 2:
+                stream.wait_stream(out_stream)
+                t_start.record(stream)
+            for dt, ht in ins:
+                dt.copy_(ht, non_blocking=True)
+            if out_done is not None:
+                stream.wait_event(out_done)
+            for fn in launches:
+                fn()
+            computed = torch.cuda.Event()
+            computed.record(stream)
+            out_stream.wait_event(computed)
+            with torch.cuda.stream(out_stream):
+                for dt, ht in outs:
+                    ht.copy_(dt, non_blocking=True)
+                out_done = torch.cuda.Event()
+                out_done.record(out_stream)
+        stream.wait_event(out_done)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        e2e_overlap = "step i's device-to-host read-back runs beside step i+1's host-to-device copies"
+    h2d = sum(t.numel() * t.element_size() for t, _ in ins)
+    d2h = sum(t.numel() * t.element_size() for t, _ in outs)
     e2e_ms = t_start.elapsed_time(t_end) / e2e_steps
     e2e_ms = max_over_ranks(torch, dist, e2e_ms, "cuda")
     e2e_value = whole_job_tflops(world, flops_step, e2e_ms)
@@ -1071,7 +1136,7 @@ def run_gpu(args):
         "clocks": sampler.summary(t_wall0, t_wall1),
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "overlap": "step i's device-to-host read-back runs beside step i+1's host-to-device copies"},
+                "overlap": e2e_overlap},
         "gpu_launches": gpu_launches,
         "cpu_baseline": None,
     }
