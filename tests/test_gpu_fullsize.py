@@ -234,3 +234,37 @@ def test_fp4_contiguous_swiglu_full_size(fg):
     q_ref, sf_ref = S.swiglu_quantize(h)
     sf = _sf_bytes(sfq.cpu().numpy(), m_total, inter // 128)[rows]
     compare_quantised(qh[rows], sf, q_ref, sf_ref, _y_ref(h), "fp4 contiguous swiglu full size")
+
+
+@pytest.mark.parametrize("weights", ["fp8", "fp4"])
+def test_masked_swiglu_full_size(fg, weights):
+    """The fused gate-up GEMM in the masked layout at the masked benchmark shape read as gate
+    + up (32 experts x 256 rows, B [32, 2 x 2048, 2048]): sampled rows of every expert
+    against the oracle, rows past each mask untouched."""
+    from gpu_util import dev
+    from oracle import fp4 as FP4
+    from oracle import swiglu as S
+    from test_gpu_swiglu import SENT_Q, _sf_bytes, _y_ref, compare_quantised
+    case = C.masked_case(1015, weights=weights)
+    g_, m_max, inter = case["g"], case["m_max"], case["n"] // 2
+    q = torch.full((g_, m_max, inter), SENT_Q, dtype=torch.uint8, device="cuda")
+    sfq = torch.zeros((g_, (inter + 511) // 512, (m_max + 3) // 4 * 4), dtype=torch.int32, device="cuda")
+    call = fg.m_grouped_fp8_fp4_gemm_nt_masked_swiglu if weights == "fp4" else fg.m_grouped_fp8_gemm_nt_masked_swiglu
+    call(dev(case["a"]), dev(case["sfa"]), dev(case["b"]), dev(case["sfb"]), dev(case["masked_m"]), q, sfq)
+    _ok(fg)
+    qh, sfh = q.cpu().numpy(), sfq.cpu().numpy()
+    g = np.random.Generator(np.random.PCG64(16))
+    rows = {}
+    for e in range(g_):
+        mm = int(case["masked_m"][e])
+        assert np.all(qh[e, mm:] == SENT_Q), f"group {e}: rows beyond the mask written"
+        pick = set(g.choice(mm, size=min(mm, 4), replace=False).tolist()) if mm > 0 else set()
+        rows[e] = np.array(sorted(pick | ({0, mm - 1} if mm > 0 else set())), dtype=np.int64)
+    ref_gemm = FP4.m_grouped_fp8_fp4_gemm_nt_masked if weights == "fp4" else C.oracle.m_grouped_fp8_gemm_nt_masked
+    hs = ref_gemm(case["a"], case["sfa"], case["b"], case["sfb"], case["masked_m"], rows=rows)
+    for e in range(g_):
+        if len(rows[e]) == 0:
+            continue
+        q_ref, sf_ref = S.swiglu_quantize(hs[e])
+        sf = _sf_bytes(sfh[e], m_max, inter // 128)[rows[e]]
+        compare_quantised(qh[e, rows[e]], sf, q_ref, sf_ref, _y_ref(hs[e]), f"masked swiglu {weights} group {e}")
