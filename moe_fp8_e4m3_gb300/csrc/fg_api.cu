@@ -207,8 +207,10 @@ int forced_split() {
 // output) it is not considered.  Measured on GB300: 4096 x 7168 x 2048 FP32 D without C,
 // BN=224 67 us against BN=256 74 us; BF16 D, masked 32 x 256 x 4096 x 2048 62.1 us against
 // 63.9 us and contiguous 32 x 4096 x 4096 137.9 us against 140.2 us.  Where two widths cost
-// the same, the order of the list decides: the same GEMM with an FP32 C (7 waves of 224 or 8
-// of 192) ran 76.6 us at BN=224, 80.3 us at 192 and 82.0 us at 128.
+// the same, the one whose last wave leaves fewer SMs idle is taken (then the order of the
+// list): the same GEMM with an FP32 C, 7 waves of 224 (the last one 112 tiles) or exactly 8
+// of 192, ran 70.8 us at BN=224 and 69.7 us at 192 as the first GEMM of the dense pair (step
+// 1467 against 1485 TFLOP/s over ten runs each; 73.7 against 74.0 us alone).
 // The FP8 x FP4 variants exist at two widths, 128 and 224 (fp4 restricts the choice to them).
 bool fp4_width(int bn) { return bn == 128 || bn == 224; }
 
@@ -217,13 +219,19 @@ int choose_bn_nt(long long row_blocks, int n, int sms, bool heavy_epilogue, bool
     if ((f == 64 || f == 128 || f == 192 || f == 224 || f == 256) && (!fp4 || fp4_width(f))) return f;
     int best = 128;
     double best_cost = -1.0;
+    long long best_idle = 0;
     for (int bn : {224, 256, 192, 128, 64}) {
         if (heavy_epilogue && bn == 256) continue;
         if (fp4 && !fp4_width(bn)) continue;
         const long long tiles = row_blocks * ceil_div(n, bn);
         const long long waves = (tiles + sms - 1) / sms;
+        const long long idle = waves * sms - tiles;     // SMs without a tile in the last wave
         const double cost = static_cast<double>(waves * (bn + 32)) * (bn == 256 ? 1.15 : 1.0);
-        if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+        if (best_cost < 0 || cost < best_cost || (cost == best_cost && idle < best_idle)) {
+            best = bn;
+            best_cost = cost;
+            best_idle = idle;
+        }
     }
     return best;
 }

@@ -1,8 +1,9 @@
 """The tile choices of the benchmark shapes on a 152-SM GB300.
 
 The host cost model picks the N tile (and, for dense GEMMs with few tiles, a split-K
-cluster) per call.  These choices carry most of the measured performance (for instance
-BN=224 with two TMEM accumulators against BN=256 with one on the M-grouped GEMMs), so a
+cluster) per call.  These choices carry much of the measured performance (for instance
+BN=224 with two TMEM accumulators against BN=256 with one on the M-grouped GEMMs, and 192
+against 224 on the prefill, where the model's costs tie and whole waves decide), so a
 change to the model that moves them should be deliberate: each benchmark shape is launched
 once with FG_PRINT_CONFIGS=1 (zero operands; only the printed choice is checked here, the
 results are covered by the parity tests)."""
@@ -57,7 +58,7 @@ def _dense(fg, m, n, k, with_c, out):
 
 
 @pytest.mark.parametrize("m,n,k,with_c,out,bn,split", [
-    (4096, 7168, 2048, True, "f32", 224, 1),    # the prefill
+    (4096, 7168, 2048, True, "f32", 192, 1),    # the prefill: 8 whole waves (224: 7, the last partial)
     (64, 7168, 4096, True, "f32", 128, 2),      # the decode: 2-CTA split-K clusters
     (128, 256, 512, False, "bf16", 64, 1),      # the small case: unsplit
 ])
