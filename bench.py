@@ -28,8 +28,12 @@ and of the measured ones (MEASURED_PEAKS.json copy bandwidth; BF16 burst x 2 for
 
 Other workloads (--workload prefill | decode | small | contiguous | masked | k_grouped,
 the other operand layouts prefill_nn | prefill_tn | prefill_tt | contiguous_nn, the fused
-gate-up GEMM contiguous_swiglu, and the indexer's mqa_logits) time single GEMMs on the
-same rules; they are measurement aids, the default line is the headline.
+gate-up GEMM contiguous_swiglu, the indexer's mqa_logits, the quantisers quant, the FP8 x
+FP4 forms fp4_dense_pair | fp4_prefill | fp4_decode | fp4_contiguous | fp4_masked |
+fp4_contiguous_swiglu, and the MoE expert MLP moe_mlp | fp4_moe_mlp) time them on the same
+rules; they are measurement aids, the default line is the headline (its config.kernels also
+records small, contiguous, masked, k_grouped, quant and the FP8 x FP4 dense pair,
+contiguous and masked).
 
 Output: one JSON line from rank 0 (see the keys below).  ``--impl reference`` times the
 CPU oracle instead, on full dense-pair steps (or a bounded sample of each step when
